@@ -1,0 +1,189 @@
+"""GB300 (sm_103a) multi-head attention forward: Python binding.
+
+A thin ctypes layer over ``libattn_gb300.so`` (C ABI in ``include/attn.h``).
+It only marshals arguments -- every step of the computation runs in the
+library's CUDA kernels.  PyTorch provides device memory and streams.  There is
+no fallback: if the library is not built, every call raises.
+
+Entry points (same names as the C ABI):
+
+* ``attn_fwd(q, k, v, ...)``        fused online-softmax attention
+* ``attn_fwd_naive(q, k, v, ...)``  unfused two-pass-softmax comparison path
+* ``qkv_proj_attn(x, w_qkv, h, ...)`` fused QKV projection, then attention
+* ``attn_get_device_status()``, ``attn_status_string(rc)``
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+LAYOUT_BHSD = 0  # contiguous [B, h, S, d]
+LAYOUT_BSHD = 1  # head-interleaved [B, S, h, d]
+ATTN_F32, ATTN_F16, ATTN_BF16 = 0, 1, 2
+ATTN_OK = 0
+ATTN_E_TIMEOUT = -9
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libattn_gb300.so")
+_lib = None
+_lock = threading.Lock()
+
+
+class AttnError(RuntimeError):
+    def __init__(self, rc: int, what: str):
+        self.rc = rc
+        super().__init__(f"{what} failed: {attn_status_string(rc)} (status {rc})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, ci, cf, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+            L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, cf, ci, ci, vp]
+            L.attn_fwd.restype = ci
+            L.attn_fwd_naive.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, cf, ci, ci, vp, sz, vp]
+            L.attn_fwd_naive.restype = ci
+            L.attn_fwd_naive_workspace_bytes.argtypes = [ci, ci, ci, ci]
+            L.attn_fwd_naive_workspace_bytes.restype = sz
+            L.qkv_proj_attn.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, vp, sz, vp]
+            L.qkv_proj_attn.restype = ci
+            L.qkv_proj_attn_workspace_bytes.argtypes = [ci, ci, ci, ci]
+            L.qkv_proj_attn_workspace_bytes.restype = sz
+            L.attn_status_string.argtypes = [ci]
+            L.attn_status_string.restype = ctypes.c_char_p
+            L.attn_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
+            L.attn_get_device_status.restype = ci
+            L.attn_abi_version.argtypes = []
+            L.attn_abi_version.restype = ci
+            _lib = L
+    return _lib
+
+
+def attn_status_string(rc: int) -> str:
+    return lib().attn_status_string(int(rc)).decode()
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def dtype_code(dt) -> int:
+    torch = _torch()
+    codes = {torch.float32: ATTN_F32, torch.float16: ATTN_F16, torch.bfloat16: ATTN_BF16}
+    if dt not in codes:
+        raise TypeError(f"unsupported dtype {dt}")
+    return codes[dt]
+
+
+def _stream_ptr(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dims(q, layout):
+    if q.dim() != 4:
+        raise ValueError("q must be 4-d")
+    if layout == LAYOUT_BHSD:
+        B, h, S, d = q.shape
+    elif layout == LAYOUT_BSHD:
+        B, S, h, d = q.shape
+    else:
+        raise ValueError("layout must be 0 ([B,h,S,d]) or 1 ([B,S,h,d])")
+    return int(B), int(h), int(S), int(d)
+
+
+def _check_dense(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def _ptr(t):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def attn_fwd(q, k, v, o=None, lse=None, *, layout: int = LAYOUT_BHSD, scale: float | None = None,
+             want_lse: bool = False, stream=None):
+    """O = softmax(scale·Q·K^T)·V (fused, one launch).  Returns (o, lse or None)."""
+    torch = _torch()
+    B, h, S, d = _dims(q, layout)
+    if k.shape != q.shape or v.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share shape and dtype")
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, h, S), dtype=torch.float32, device=q.device)
+    _check_dense(q, k, v, o, lse)
+    rc = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, h, S, d,
+                        float(scale) if scale else 0.0, layout, dtype_code(q.dtype), _stream_ptr(stream))
+    if rc:
+        raise AttnError(rc, "attn_fwd")
+    return o, lse
+
+
+def attn_fwd_naive_workspace_bytes(B: int, h: int, S: int, dtype) -> int:
+    return int(lib().attn_fwd_naive_workspace_bytes(B, h, S, dtype_code(dtype)))
+
+
+def attn_fwd_naive(q, k, v, o=None, lse=None, workspace=None, *, layout: int = LAYOUT_BHSD,
+                   scale: float | None = None, want_lse: bool = False, stream=None):
+    """Unfused comparison path (S and P materialised).  Returns (o, lse or None, workspace)."""
+    torch = _torch()
+    B, h, S, d = _dims(q, layout)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, h, S), dtype=torch.float32, device=q.device)
+    need = attn_fwd_naive_workspace_bytes(B, h, S, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check_dense(q, k, v, o, lse, workspace)
+    rc = lib().attn_fwd_naive(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, h, S, d,
+                              float(scale) if scale else 0.0, layout, dtype_code(q.dtype),
+                              _ptr(workspace), workspace.numel() * workspace.element_size(),
+                              _stream_ptr(stream))
+    if rc:
+        raise AttnError(rc, "attn_fwd_naive")
+    return o, lse, workspace
+
+
+def qkv_proj_attn_workspace_bytes(B: int, S: int, D: int, dtype) -> int:
+    return int(lib().qkv_proj_attn_workspace_bytes(B, S, D, dtype_code(dtype)))
+
+
+def qkv_proj_attn(x, w_qkv, h: int, o=None, workspace=None, *, stream=None):
+    """X [B,S,D] · W_qkv [D,3D] -> heads -> attention.  Returns (o [B,S,h,d], workspace [B,S,3D] bytes)."""
+    torch = _torch()
+    B, S, D = (int(n) for n in x.shape)
+    if o is None:
+        o = torch.empty((B, S, h, D // h), dtype=x.dtype, device=x.device)
+    need = qkv_proj_attn_workspace_bytes(B, S, D, x.dtype)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    _check_dense(x, w_qkv, o, workspace)
+    rc = lib().qkv_proj_attn(_ptr(x), _ptr(w_qkv), _ptr(o), B, S, D, h, dtype_code(x.dtype),
+                             _ptr(workspace), workspace.numel() * workspace.element_size(),
+                             _stream_ptr(stream))
+    if rc:
+        raise AttnError(rc, "qkv_proj_attn")
+    return o, workspace
+
+
+def attn_get_device_status(stream=None) -> tuple[int, int]:
+    """Synchronise the stream; return (status, raw detail) and clear the device status word."""
+    detail = ctypes.c_uint(0)
+    rc = lib().attn_get_device_status(_stream_ptr(stream), ctypes.byref(detail))
+    return int(rc), int(detail.value)

@@ -1,0 +1,402 @@
+// C ABI of libattn_gb300.so (declared in include/attn.h): argument
+// validation, TMA tensor-map encoding, kernel selection and launch.
+//
+// Every argument is checked before the first CUDA call, so an invalid call
+// returns a negative ATTN_E_* code without touching the device.
+
+#include <math.h>
+#include <stdlib.h>
+
+#include <mutex>
+
+#include "attn.h"
+#include "common.h"
+
+namespace {
+
+// One status word per device; kernels record a pipeline timeout here.
+__device__ unsigned g_status;
+
+constexpr int kMaxDevices = 64;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct DeviceState {
+  bool ready = false;
+  int rc = ATTN_OK;
+  unsigned* status = nullptr;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+EncodeTiledFn g_encode = nullptr;
+
+int elt_bytes(int dtype) { return dtype == ATTN_F32 ? 4 : 2; }
+
+// Resolves the per-device state of the current device: sm_103 check, address
+// of the status word and the driver's tensor-map encoder.
+int device_setup(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_E_DEVICE;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    st.ready = true;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        major != 10 || minor != 3) {
+      st.rc = ATTN_E_DEVICE;
+    } else if (cudaGetSymbolAddress(reinterpret_cast<void**>(&st.status), g_status) != cudaSuccess) {
+      st.rc = ATTN_E_DEVICE;
+    } else if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        st.rc = ATTN_E_DEVICE;
+      else
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+  }
+  *out = &st;
+  return st.rc;
+}
+
+// Clock cycles a pipeline wait may take before the kernel gives up
+// (default 4e9, about two seconds at GB300 clocks; ATTN_WAIT_LIMIT_CYCLES overrides).
+long long wait_limit() {
+  static long long v = [] {
+    const char* s = getenv("ATTN_WAIT_LIMIT_CYCLES");
+    long long x = s ? atoll(s) : 0;
+    return x > 0 ? x : 4000000000LL;
+  }();
+  return v;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+// 4-d tensor map over a [B, H, S, d] problem in either layout.  `rs` is the
+// row stride in elements (distance between consecutive positions s of one
+// head in layout 1; ignored in layout 0).  Box: 64 features x box_rows rows.
+int make_map(CUtensorMap* m, const void* base, int dtype, int layout, long long B, long long H,
+             long long S, long long d, long long rs, int box_rows, int* hs_swap) {
+  const cuuint64_t e = static_cast<cuuint64_t>(elt_bytes(dtype));
+  cuuint64_t dims[4], strides[3];
+  cuuint32_t box[4], estr[4] = {1, 1, 1, 1};
+  if (layout == ATTN_LAYOUT_BHSD) {  // dims (d, S, H, B)
+    dims[0] = d, dims[1] = S, dims[2] = H, dims[3] = B;
+    strides[0] = d * e, strides[1] = S * d * e, strides[2] = H * S * d * e;
+    box[0] = 64, box[1] = box_rows, box[2] = 1, box[3] = 1;
+    *hs_swap = 0;
+  } else {  // dims (d, H, S, B)
+    dims[0] = d, dims[1] = H, dims[2] = S, dims[3] = B;
+    strides[0] = d * e, strides[1] = rs * e, strides[2] = S * rs * e;
+    box[0] = 64, box[1] = 1, box[2] = box_rows, box[3] = 1;
+    *hs_swap = 1;
+  }
+  const CUtensorMapDataType dt =
+      dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUresult r = g_encode(m, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_E_DEVICE;
+}
+
+// Plain row-major matrices [Z2][Z1][rows][cols] with row stride ld (elements)
+// as a 4-d map (cols, rows, Z1, Z2); box 64 x box_rows.
+int make_matrix_map(CUtensorMap* m, const void* base, int dtype, long long Z1, long long Z2,
+                    long long rows, long long cols, long long ld, int box_rows) {
+  const cuuint64_t e = static_cast<cuuint64_t>(elt_bytes(dtype));
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(Z1), static_cast<cuuint64_t>(Z2)};
+  cuuint64_t strides[3] = {ld * e, rows * ld * e, Z1 * rows * ld * e};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1, 1}, estr[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType dt =
+      dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUresult r = g_encode(m, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_E_DEVICE;
+}
+
+int to_rc(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : static_cast<int>(e); }
+
+// Checks shared by attn_fwd and attn_fwd_naive.  Makes no CUDA call.
+int validate_attn(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                  int B, int h, int S, int d, int layout, int dtype) {
+  if (!q || !k || !v || !o) return ATTN_E_NULL;
+  if (layout != ATTN_LAYOUT_BHSD && layout != ATTN_LAYOUT_BSHD) return ATTN_E_LAYOUT;
+  if (dtype != ATTN_F32 && dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_E_DTYPE;
+  if (B < 1 || h < 1 || S < 1 || d < 1) return ATTN_E_SHAPE;
+  if (dtype == ATTN_F32 ? d > 256 : (d != 64 && d != 128)) return ATTN_E_SHAPE;
+  const long long elems = static_cast<long long>(B) * h * S * d;
+  if (elems > (1LL << 40)) return ATTN_E_SHAPE;
+  const long long ctas = static_cast<long long>(B) * h * ((S + 255) / 256);
+  if (ctas > 0x7fffffffLL || static_cast<long long>(B) * h * ((S + 7) / 8) > 0x7fffffffLL)
+    return ATTN_E_SHAPE;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      (lse && !aligned(lse, 4)))
+    return ATTN_E_ALIGN;
+  const size_t bytes = static_cast<size_t>(elems) * elt_bytes(dtype);
+  if (overlap(o, bytes, q, bytes) || overlap(o, bytes, k, bytes) || overlap(o, bytes, v, bytes))
+    return ATTN_E_ALIAS;
+  if (lse) {
+    const size_t lb = static_cast<size_t>(B) * h * S * sizeof(float);
+    if (overlap(lse, lb, q, bytes) || overlap(lse, lb, k, bytes) || overlap(lse, lb, v, bytes) ||
+        overlap(lse, lb, o, bytes))
+      return ATTN_E_ALIAS;
+  }
+  return ATTN_OK;
+}
+
+void o_strides(int layout, long long H, long long S, long long d, long long rs, long long* sb,
+               long long* sh, long long* ss) {
+  if (layout == ATTN_LAYOUT_BHSD) {
+    *ss = d, *sh = S * d, *sb = H * S * d;
+  } else {
+    *sh = d, *ss = rs, *sb = S * rs;
+  }
+}
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Flash launch on tensors of a [B,H,S,d] problem with row stride rs (layout 1).
+int run_flash(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h, int S,
+              int d, float scale, int layout, int dtype, long long rs_in, long long rs_out,
+              unsigned* status, cudaStream_t st) {
+  attn::FlashLaunch a;
+  int swap = 0;
+  int rc = make_map(&a.tq, q, dtype, layout, B, h, S, d, rs_in, 128, &swap);
+  if (!rc) rc = make_map(&a.tk, k, dtype, layout, B, h, S, d, rs_in, 128, &swap);
+  if (!rc) rc = make_map(&a.tv, v, dtype, layout, B, h, S, d, rs_in, 128, &swap);
+  if (rc) return rc;
+  a.o = o;
+  a.lse = lse;
+  o_strides(layout, h, S, d, rs_out, &a.o_sb, &a.o_sh, &a.o_ss);
+  a.B = B, a.H = h, a.S = S, a.d = d;
+  a.hs_swap = swap;
+  a.bf16 = dtype == ATTN_BF16;
+  a.scale = scale;
+  a.status = status;
+  a.limit = wait_limit();
+  return to_rc(attn::launch_flash_fwd(a, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_abi_version(void) { return 1; }
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h, int S,
+             int d, float scale, int layout, int dtype, void* stream) {
+  int rc = validate_attn(q, k, v, o, lse, B, h, S, d, layout, dtype);
+  if (rc) return rc;
+  DeviceState* ds = nullptr;
+  if ((rc = device_setup(&ds))) return rc;
+  const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(d));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dtype == ATTN_F32) {
+    attn::SimtLaunch a;
+    a.q = static_cast<const float*>(q);
+    a.k = static_cast<const float*>(k);
+    a.v = static_cast<const float*>(v);
+    a.o = static_cast<float*>(o);
+    a.lse = lse;
+    o_strides(layout, h, S, d, static_cast<long long>(h) * d, &a.sb, &a.sh, &a.ss);
+    a.B = B, a.H = h, a.S = S, a.d = d;
+    a.scale = sc;
+    return to_rc(attn::launch_simt_fwd(a, st));
+  }
+  const long long rs = static_cast<long long>(h) * d;
+  return run_flash(q, k, v, o, lse, B, h, S, d, sc, layout, dtype, rs, rs, ds->status, st);
+}
+
+size_t attn_fwd_naive_workspace_bytes(int B, int h, int S, int dtype) {
+  if (B < 1 || h < 1 || S < 1 || (dtype != ATTN_F16 && dtype != ATTN_BF16)) return 0;
+  const size_t rows = static_cast<size_t>(B) * h * S;
+  const size_t sp = (static_cast<size_t>(S) + 7) & ~static_cast<size_t>(7);
+  return round256(rows * sp * 4) + round256(rows * sp * 2) + 2 * round256(rows * 4);
+}
+
+int attn_fwd_naive(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h,
+                   int S, int d, float scale, int layout, int dtype, void* workspace,
+                   size_t ws_bytes, void* stream) {
+  int rc = validate_attn(q, k, v, o, lse, B, h, S, d, layout, dtype);
+  if (rc) return rc;
+  if (dtype == ATTN_F32) return ATTN_E_DTYPE;
+  const size_t need = attn_fwd_naive_workspace_bytes(B, h, S, dtype);
+  if (!workspace || ws_bytes < need || !aligned(workspace, 256)) return ATTN_E_WORKSPACE;
+  const size_t bytes = static_cast<size_t>(B) * h * S * d * 2;
+  if (overlap(workspace, need, q, bytes) || overlap(workspace, need, k, bytes) ||
+      overlap(workspace, need, v, bytes) || overlap(workspace, need, o, bytes) ||
+      (lse && overlap(workspace, need, lse, static_cast<size_t>(B) * h * S * 4)))
+    return ATTN_E_ALIAS;
+  DeviceState* ds = nullptr;
+  if ((rc = device_setup(&ds))) return rc;
+  const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(d));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const long long rows = static_cast<long long>(B) * h * S;
+  const long long sp = (static_cast<long long>(S) + 7) & ~7LL;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* s_mat = reinterpret_cast<float*>(ws);
+  void* p_mat = ws + round256(rows * sp * 4);
+  float* m_vec = reinterpret_cast<float*>(ws + round256(rows * sp * 4) + round256(rows * sp * 2));
+  float* l_vec = m_vec + round256(rows * 4) / 4;
+  const long long rs = static_cast<long long>(h) * d;
+
+  // 1. S = scale · Q·K^T  (fp32, [B,H,S,sp])
+  attn::GemmLaunch g1;
+  int swap = 0;
+  rc = make_map(&g1.ta, q, dtype, layout, B, h, S, d, rs, 128, &swap);
+  if (!rc) rc = make_map(&g1.tb, k, dtype, layout, B, h, S, d, rs, 128, &swap);
+  if (rc) return rc;
+  g1.c = s_mat;
+  g1.c_type = 0;
+  g1.ldc = sp;
+  g1.c_s1 = S * sp;
+  g1.c_s2 = static_cast<long long>(h) * S * sp;
+  g1.M = S, g1.N = S, g1.K = d, g1.Z1 = h, g1.Z2 = B;
+  g1.bn = 128;
+  g1.b_kmajor = true;
+  g1.a_swap = g1.b_swap = swap;
+  g1.bf16 = dtype == ATTN_BF16;
+  g1.alpha = sc;
+  g1.status = ds->status;
+  g1.limit = wait_limit();
+  if ((rc = to_rc(attn::launch_gemm(g1, st)))) return rc;
+
+  // 2.-3. row statistics, then P = exp(S - m) / l
+  attn::NaiveSoftmaxLaunch sm;
+  sm.s = s_mat;
+  sm.p = p_mat;
+  sm.m = m_vec;
+  sm.l = l_vec;
+  sm.lse = lse;
+  sm.rows = rows;
+  sm.n = S;
+  sm.ld = sp;
+  sm.bf16 = dtype == ATTN_BF16;
+  if ((rc = to_rc(attn::launch_naive_softmax(sm, st)))) return rc;
+
+  // 4. O = P·V
+  attn::GemmLaunch g2;
+  rc = make_matrix_map(&g2.ta, p_mat, dtype, h, B, S, S, sp, 128);
+  if (!rc) rc = make_map(&g2.tb, v, dtype, layout, B, h, S, d, rs, 64, &swap);
+  if (rc) return rc;
+  g2.c = o;
+  g2.c_type = dtype;
+  o_strides(layout, h, S, d, rs, &g2.c_s2, &g2.c_s1, &g2.ldc);
+  g2.M = S, g2.N = d, g2.K = S, g2.Z1 = h, g2.Z2 = B;
+  g2.bn = d;
+  g2.b_kmajor = false;
+  g2.a_swap = 0;
+  g2.b_swap = swap;
+  g2.bf16 = dtype == ATTN_BF16;
+  g2.alpha = 1.f;
+  g2.status = ds->status;
+  g2.limit = wait_limit();
+  return to_rc(attn::launch_gemm(g2, st));
+}
+
+size_t qkv_proj_attn_workspace_bytes(int B, int S, int D, int dtype) {
+  if (B < 1 || S < 1 || D < 1 || (dtype != ATTN_F16 && dtype != ATTN_BF16)) return 0;
+  return round256(static_cast<size_t>(B) * S * 3 * D * 2);
+}
+
+int qkv_proj_attn(const void* x, const void* w_qkv, void* o, int B, int S, int D, int h, int dtype,
+                  void* workspace, size_t ws_bytes, void* stream) {
+  if (!x || !w_qkv || !o) return ATTN_E_NULL;
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_E_DTYPE;
+  if (B < 1 || S < 1 || h < 1 || D < 1 || D % h) return ATTN_E_SHAPE;
+  const int d = D / h;
+  if (d != 64 && d != 128) return ATTN_E_SHAPE;
+  const long long rows = static_cast<long long>(B) * S;
+  if (rows * 3 * D > (1LL << 40) || static_cast<long long>(B) * h * ((S + 255) / 256) > 0x7fffffffLL ||
+      ((rows + 127) / 128) * ((3LL * D + 127) / 128) > 0x7fffffffLL)
+    return ATTN_E_SHAPE;
+  if (!aligned(x, 16) || !aligned(w_qkv, 16) || !aligned(o, 16)) return ATTN_E_ALIGN;
+  const size_t need = qkv_proj_attn_workspace_bytes(B, S, D, dtype);
+  if (!workspace || ws_bytes < need || !aligned(workspace, 256)) return ATTN_E_WORKSPACE;
+  const size_t xb = static_cast<size_t>(rows) * D * 2, wb = static_cast<size_t>(D) * 3 * D * 2;
+  if (overlap(o, xb, x, xb) || overlap(o, xb, w_qkv, wb) || overlap(o, xb, workspace, need) ||
+      overlap(workspace, need, x, xb) || overlap(workspace, need, w_qkv, wb))
+    return ATTN_E_ALIAS;
+  DeviceState* ds = nullptr;
+  int rc = device_setup(&ds);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  // 1. QKV = X · W_qkv  -> workspace [B·S, 3D]
+  attn::GemmLaunch g;
+  rc = make_matrix_map(&g.ta, x, dtype, 1, 1, rows, D, D, 128);
+  if (!rc) rc = make_matrix_map(&g.tb, w_qkv, dtype, 1, 1, D, 3LL * D, 3LL * D, 64);
+  if (rc) return rc;
+  g.c = workspace;
+  g.c_type = dtype;
+  g.ldc = 3LL * D;
+  g.c_s1 = g.c_s2 = 0;
+  g.M = static_cast<int>(rows), g.N = 3 * D, g.K = D, g.Z1 = 1, g.Z2 = 1;
+  g.bn = 128;
+  g.b_kmajor = false;
+  g.a_swap = g.b_swap = 0;
+  g.bf16 = dtype == ATTN_BF16;
+  g.alpha = 1.f;
+  g.status = ds->status;
+  g.limit = wait_limit();
+  if (rows > 0x7fffffffLL) return ATTN_E_SHAPE;
+  if ((rc = to_rc(attn::launch_gemm(g, st)))) return rc;
+
+  // 2. attention on the projection in place: Q, K, V are the three column
+  //    blocks of each row, i.e. head-interleaved with row stride 3D.
+  const uint8_t* base = static_cast<const uint8_t*>(workspace);
+  return run_flash(base, base + static_cast<size_t>(D) * 2, base + static_cast<size_t>(2 * D) * 2, o,
+                   nullptr, B, h, S, d, 1.0f / sqrtf(static_cast<float>(d)), ATTN_LAYOUT_BSHD, dtype,
+                   3LL * D, D, ds->status, st);
+}
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_E_NULL: return "ATTN_E_NULL: a required pointer is NULL";
+    case ATTN_E_SHAPE: return "ATTN_E_SHAPE: unsupported or inconsistent sizes";
+    case ATTN_E_ALIGN: return "ATTN_E_ALIGN: tensor pointer not 16-byte aligned";
+    case ATTN_E_LAYOUT: return "ATTN_E_LAYOUT: unknown layout";
+    case ATTN_E_DTYPE: return "ATTN_E_DTYPE: unknown or unsupported dtype";
+    case ATTN_E_WORKSPACE: return "ATTN_E_WORKSPACE: workspace missing, misaligned or too small";
+    case ATTN_E_ALIAS: return "ATTN_E_ALIAS: output overlaps an input or the workspace";
+    case ATTN_E_DEVICE: return "ATTN_E_DEVICE: no usable sm_103 device or driver entry point";
+    case ATTN_E_TIMEOUT: return "ATTN_E_TIMEOUT: a kernel pipeline wait exceeded its limit";
+    default: break;
+  }
+  if (status > 0) return cudaGetErrorString(static_cast<cudaError_t>(status));
+  return "unknown attn status";
+}
+
+int attn_get_device_status(void* stream, unsigned int* detail) {
+  if (detail) *detail = 0;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return static_cast<int>(e);
+  DeviceState* ds = nullptr;
+  int rc = device_setup(&ds);
+  if (rc) return rc;
+  unsigned v = 0, zero = 0;
+  if ((e = cudaMemcpy(&v, ds->status, sizeof v, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return static_cast<int>(e);
+  if ((e = cudaMemcpy(ds->status, &zero, sizeof zero, cudaMemcpyHostToDevice)) != cudaSuccess)
+    return static_cast<int>(e);
+  if (detail) *detail = v;
+  return v ? ATTN_E_TIMEOUT : ATTN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,77 @@
+// Host-side interfaces between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace attn {
+
+// Tensor-map dimension order for a [B, H, S, d] problem:
+//   hs_swap = 0: dims (d, S, H, B)  -- contiguous layout [B,H,S,d]
+//   hs_swap = 1: dims (d, H, S, B)  -- head-interleaved layout [B,S,H,d]
+// so that the byte strides always grow with the dimension index.
+
+struct FlashLaunch {
+  CUtensorMap tq, tk, tv;       // 4-d maps, box = 64 features x 128 rows
+  void* o;                      // output, element strides below (feature stride 1)
+  float* lse;                   // [B,H,S] fp32 or null
+  long long o_sb, o_sh, o_ss;
+  int B, H, S, d;
+  int hs_swap;
+  bool bf16;
+  float scale;                  // softmax scale (already resolved)
+  unsigned* status;             // device status word
+  long long limit;              // clock cycles per wait before giving up
+};
+cudaError_t launch_flash_fwd(const FlashLaunch& a, cudaStream_t st);
+
+struct SimtLaunch {
+  const float *q, *k, *v;
+  float* o;
+  float* lse;
+  long long sb, sh, ss;         // element strides shared by q, k, v, o
+  int B, H, S, d;
+  float scale;
+};
+cudaError_t launch_simt_fwd(const SimtLaunch& a, cudaStream_t st);
+
+// Batched tensor-core GEMM   C[z] = alpha · A[z] · op(B[z])
+//   A: [M, K] K-major (4-d map: K, M, Z1, Z2; box 64 x 128)
+//   B: b_kmajor ? [N, K] (map: K, N, Z1, Z2; box 64 x BN)
+//              : [K, N] (map: N, K, Z1, Z2; box 64 x 64)
+//   z in [0, Z1·Z2): operand coordinates (z % Z1, z / Z1)
+//   C element (z, m, n) at c + (z / Z1)·c_s2 + (z % Z1)·c_s1 + m·ldc + n
+struct GemmLaunch {
+  CUtensorMap ta, tb;
+  void* c;
+  int c_type;                   // 0 = fp32, 1 = fp16, 2 = bf16
+  long long ldc, c_s1, c_s2;
+  int M, N, K, Z1, Z2;
+  int bn;                       // 64 or 128
+  bool b_kmajor;
+  int a_swap, b_swap;           // 1: map dims are (inner, Z1, rows, Z2) instead of (inner, rows, Z1, Z2)
+  bool bf16;                    // operand type
+  float alpha;
+  unsigned* status;
+  long long limit;
+};
+cudaError_t launch_gemm(const GemmLaunch& a, cudaStream_t st);
+
+// Naive softmax passes over an fp32 score matrix [rows, n] (row stride ld):
+//   pass 1: stats[r] = (max_j S[r,j], sum_j exp(S[r,j] - max))
+//   pass 2: P[r,j] = exp(S[r,j] - m_r) / l_r  (16-bit), and lse[...] if asked
+struct NaiveSoftmaxLaunch {
+  const float* s;               // row stride ld (fp32 elements)
+  void* p;                      // dtype of the attention
+  float* m;                     // [rows]
+  float* l;                     // [rows]
+  float* lse;                   // [B,H,S] or null (rows are ordered (b, h, i))
+  long long rows;
+  int n;
+  long long ld;                 // row stride of s and p, in elements
+  bool bf16;
+};
+cudaError_t launch_naive_softmax(const NaiveSoftmaxLaunch& a, cudaStream_t st);
+
+}  // namespace attn

@@ -1,0 +1,153 @@
+/*
+ * attn.h -- C ABI of libattn_gb300.so, the GB300 (sm_103a) multi-head
+ * attention forward.
+ *
+ * The operation is O = softmax(scale · Q·K^T) · V per (batch, head), taken
+ * from "Transformer算子生态深度分析" chapter 2 (自注意力机制算子): scores in
+ * §2.2, row-wise softmax in §2.3, weighted sum in §2.4.  attn_fwd computes it
+ * tile by tile with the online-softmax merge of §2.6 (running max m and
+ * running exp-sum, previous output rescaled by exp(m_old - m)), so the S×S
+ * score and probability matrices never reach device memory.
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *    library keeps no reference to them after the call is enqueued and
+ *    allocates no device memory of its own (it holds one 4-byte status word
+ *    per device, a statically declared device variable).
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream).  None of them synchronises, except
+ *    attn_get_device_status.
+ *  - Element types (`dtype`): ATTN_F32, ATTN_F16, ATTN_BF16.  q, k, v, o
+ *    share one dtype.  16-bit inputs are multiplied on the tensor cores with
+ *    fp32 accumulation; softmax statistics are fp32 (the mixed-precision
+ *    split of "WebGPU 算子优化：QKV 内存合并与 FlashAttention 分块计算",
+ *    §浏览器端落地的关键参数与监控).  ATTN_F32 runs exact fp32 FMA arithmetic.
+ *  - Layouts (`layout`), from the same WebGPU page, §QKV 矩阵的内存合并模式选择:
+ *      ATTN_LAYOUT_BHSD  contiguous        [B, h, S, d]
+ *      ATTN_LAYOUT_BSHD  head-interleaved  [B, S, h, d]
+ *    q, k, v and o all use the given layout, densely packed.
+ *  - lse (optional, may be NULL) is fp32 [B, h, S]: the natural-log
+ *    log-sum-exp of each query row's scaled scores, in both layouts.
+ *  - `scale` <= 0 selects the default 1/sqrt(d) ("Transformer算子生态深度分析"
+ *    §2.2, variance argument).
+ *  - Return value: ATTN_OK (0) when the work was enqueued; a negative
+ *    ATTN_E_* code when an argument is invalid, in which case nothing was
+ *    launched and no CUDA call was made; a positive value is a cudaError_t
+ *    reported by the runtime while enqueuing.
+ *  - Device-side faults of the pipeline (a wait that exceeded its time
+ *    limit) do not trap: the kernel records a code in the device status
+ *    word and returns; read it with attn_get_device_status.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { ATTN_LAYOUT_BHSD = 0, ATTN_LAYOUT_BSHD = 1 } attn_layout;
+typedef enum { ATTN_F32 = 0, ATTN_F16 = 1, ATTN_BF16 = 2 } attn_dtype;
+
+enum {
+  ATTN_OK = 0,
+  ATTN_E_NULL = -1,      /* a required pointer is NULL                                 */
+  ATTN_E_SHAPE = -2,     /* B, h, S < 1; d unsupported for the dtype; D != h*d; too large */
+  ATTN_E_ALIGN = -3,     /* a tensor pointer is not 16-byte aligned                    */
+  ATTN_E_LAYOUT = -4,    /* layout is not ATTN_LAYOUT_BHSD / ATTN_LAYOUT_BSHD          */
+  ATTN_E_DTYPE = -5,     /* dtype unknown, or not supported by this entry point        */
+  ATTN_E_WORKSPACE = -6, /* workspace NULL, misaligned or smaller than required        */
+  ATTN_E_ALIAS = -7,     /* the output overlaps an input or the workspace              */
+  ATTN_E_DEVICE = -8,    /* no usable sm_103 device / driver entry point missing       */
+  ATTN_E_TIMEOUT = -9    /* (device status only) a pipeline wait exceeded its limit    */
+};
+
+/*
+ * attn_fwd -- fused attention forward (online softmax, one kernel launch).
+ *
+ *   q, k, v  [in]  B·h·S·d elements each, in `layout`, of `dtype`.
+ *   o        [out] same shape, layout and dtype as q.  Must not overlap q, k, v.
+ *   lse      [out] optional fp32 [B, h, S]; NULL to skip.
+ *   B, h, S, d     batch, heads, sequence length, head dimension.
+ *                  16-bit dtypes: d in {64, 128}.  ATTN_F32: 1 <= d <= 256.
+ *   scale          softmax scale; <= 0 means 1/sqrt(d).
+ *   layout, dtype  see above.
+ *   stream         cudaStream_t to enqueue on.
+ *
+ * Non-causal: every query attends to all S keys.  All pointers must be
+ * 16-byte aligned.  Errors: ATTN_E_NULL, ATTN_E_SHAPE, ATTN_E_ALIGN,
+ * ATTN_E_LAYOUT, ATTN_E_DTYPE, ATTN_E_ALIAS, ATTN_E_DEVICE, or a cudaError_t.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h, int S,
+             int d, float scale, int layout, int dtype, void* stream);
+
+/*
+ * attn_fwd_naive -- the unfused "standard" attention the pages compare
+ * against: "Transformer算子生态深度分析" §2.5 materialises S and A in device
+ * memory; the online-softmax proposal page ("[WebGPU] Proposal: Add an option
+ * to use online softmax instead of naive softmax", §三) splits the softmax
+ * into two dispatches.  Four launches:
+ *   1. S = scale · Q·K^T  -> fp32 [B, h, S, S] in the workspace (tensor cores)
+ *   2. pass 1: per row m = max S, l = sum exp(S - m)  (reads S)
+ *   3. pass 2: P = exp(S - m) / l -> dtype [B, h, S, S] in the workspace (reads S)
+ *   4. O = P·V (tensor cores)
+ * Same arguments and result as attn_fwd, 16-bit dtypes only, plus a caller
+ * workspace of at least attn_fwd_naive_workspace_bytes(B, h, S, dtype) bytes,
+ * 256-byte aligned.  On return (after the stream completes) the workspace
+ * holds S (fp32), then P (dtype), then the fp32 row statistics m and l.
+ * Errors: as attn_fwd, plus ATTN_E_WORKSPACE.
+ */
+int attn_fwd_naive(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h,
+                   int S, int d, float scale, int layout, int dtype, void* workspace,
+                   size_t ws_bytes, void* stream);
+/* Workspace size for attn_fwd_naive: B·h·S²·(4 + elt) + 2·B·h·S·4 bytes, rounded
+ * up to 256 B per part; 0 when the arguments are invalid. */
+size_t attn_fwd_naive_workspace_bytes(int B, int h, int S, int dtype);
+
+/*
+ * qkv_proj_attn -- fused QKV projection followed by attention
+ * ("Transformer算子生态深度分析" §2.1: one product with the concatenated weight
+ * [D, 3D], then split into heads; then §2.2-§2.4).
+ *
+ *   x      [in]  [B, S, D] row-major, dtype ATTN_F16 or ATTN_BF16.
+ *   w_qkv  [in]  [D, 3D] row-major; columns [0,D) produce Q, [D,2D) K,
+ *                [2D,3D) V; within each third, column c belongs to head
+ *                c / d, feature c % d (d = D / h).  No bias.
+ *   o      [out] [B, S, h, d] (head-interleaved), same dtype.
+ *   B, S, D, h   D must equal h·d with d in {64, 128}.
+ *   workspace    at least qkv_proj_attn_workspace_bytes(B, S, D, dtype)
+ *                bytes of device memory, 256-byte aligned.  On return it
+ *                holds the projection [B, S, 3D] (dtype, rounded to
+ *                nearest), i.e. Q, K, V in head-interleaved layout with row
+ *                stride 3D, which the attention kernel reads in place.
+ * Softmax scale is 1/sqrt(d).  Two launches (tensor-core GEMM, then the
+ * attn_fwd kernel).  Errors: as attn_fwd, plus ATTN_E_WORKSPACE.
+ */
+int qkv_proj_attn(const void* x, const void* w_qkv, void* o, int B, int S, int D, int h, int dtype,
+                  void* workspace, size_t ws_bytes, void* stream);
+/* Workspace size for qkv_proj_attn: B·S·3D·elt bytes rounded up to 256; 0 when invalid. */
+size_t qkv_proj_attn_workspace_bytes(int B, int S, int D, int dtype);
+
+/* Human-readable name of an ATTN_* status or a cudaError_t (positive). Never NULL. */
+const char* attn_status_string(int status);
+
+/*
+ * attn_get_device_status -- synchronises `stream`, then returns and clears
+ * the device status word of the current device: ATTN_OK, or ATTN_E_TIMEOUT
+ * when a kernel gave up on a pipeline wait (its output is then undefined), or
+ * a positive cudaError_t if the synchronisation itself failed.
+ * `detail` (may be NULL) receives the raw code the kernel recorded
+ * (kernel id << 24 | role << 16 | tile index), 0 if none.
+ */
+int attn_get_device_status(void* stream, unsigned int* detail);
+
+/* ABI version of this header: 1. */
+int attn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

@@ -1,0 +1,436 @@
+#!/usr/bin/env python3
+"""Throughput benchmark of the fused attention forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one fused attention forward (attn_fwd, one kernel launch) over the
+B=1 h=16 S=4096 d=64 fp16 workload (contiguous [B,h,S,d], non-causal, scale
+1/8).  Inputs are synthetic (seeded N(0,1)) and already resident in HBM when
+the timed region starts; 8 input sets (256 MiB in total, above the 129 MB L2)
+are rotated so that no step reads inputs another step left in L2.  Timing:
+W untimed warm-up steps, then exactly K steps between CUDA events recorded on
+the launching stream, with a barrier and a synchronize on both sides; the
+maximum over ranks is taken.  value = total FLOPs of all ranks (4·B·h·S²·d per
+step and rank) / that time.
+
+Multi-GPU (torchrun, one rank per GPU): each rank runs its own independent
+problem of the same size (the (batch, head) units of attention need no
+exchange), so per-GPU work is fixed and scaling is weak.
+
+Also reported, on rank 0:
+  roofline      achieved TFLOP/s of the attention kernel vs the measured dense
+                FP16/BF16 tensor peak, and DRAM traffic per launch from the
+                committed ncu summary (null once the kernel source changed);
+  e2e           the same metric through the C-ABI call with pinned HOST
+                buffers: every step copies Q, K, V host->device and O back;
+  cpu_baseline  the fp64 oracle timed on the host cores on a bounded sample
+                of query rows of the same workload;
+  extra         the unfused two-pass comparison path on the same workload and
+                the other workloads' fused throughput.
+``--impl reference`` times the oracle alone (CPU), on the same metric.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s (4·B·h·S²·d) & % of GB300 FP16 tensor peak, 1 GPU"
+UNIT = "TFLOP/s"
+WORKLOAD = "mha_f16_s4096"
+N_SETS = 8
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-extra", action="store_true", help="skip the comparison / other-workload lines")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------- ranks ----
+def dist_init(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks ----
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    """nvidia-smi sampling every 100 ms while the timed region runs."""
+
+    def __init__(self, gpu_index):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(gpu_index), "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.count(",") >= 8]
+        os.unlink(self.f.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]
+                          and "Not" not in r[5 + i]})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((float(r[3]) for r in rows if r[3].strip()[:1].isdigit()), default=None)}
+
+
+# ----------------------------------------------------------------- peaks ----
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS, bf16_tflops_sustained=FALLBACK_PEAKS["bf16_tflops"], source="fallback")
+
+
+def profile_traffic(kernel_hash):
+    """DRAM bytes per launch of the attention kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"flash_fwd_{WORKLOAD}.md")
+    vals = {}
+    try:
+        with open(path) as f:
+            for line in f:
+                if ":" in line and line.strip().startswith("- "):
+                    k, _, v = line.strip()[2:].partition(":")
+                    vals[k.strip()] = v.strip().strip("`")
+    except OSError:
+        return None
+    if vals.get("kernel_source_hash") != kernel_hash:
+        return None
+    try:
+        return int(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# -------------------------------------------------------------- CPU legs ----
+def oracle_rows_timing(w, q, k, v, n_rows, nthreads=0, seed=3):
+    """Times the oracle on n_rows sampled query rows; returns (seconds, flops, threads)."""
+    import oracle
+    from head_attention_fwd_gb300.inputs import sample_rows
+
+    rows = sample_rows(w, n_rows, seed=seed).numpy()
+    t0 = time.perf_counter()
+    oracle.attention_rows(q, k, v, rows, layout=w.layout, scale=w.scale, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return dt, 4.0 * w.S * w.d * len(rows), oracle.threads(nthreads)
+
+
+def cpu_baseline(w, q, k, v, budget_s=12.0):
+    """The oracle as it stands, on all host cores, on about budget_s of work."""
+    import oracle
+    cores = oracle.threads(0)
+    dt, fl, _ = oracle_rows_timing(w, q, k, v, max(cores, 32))
+    per_row = dt / max(cores, 32)
+    n = int(min(w.B * w.h * w.S, max(cores, budget_s / max(per_row, 1e-6))))
+    dt, fl, thr = oracle_rows_timing(w, q, k, v, n)
+    return {"value": fl / dt / 1e12, "unit": UNIT, "cores": thr, "kind": "oracle",
+            "sample": f"{n} of {w.B * w.h * w.S} query rows of {w.name} (seeded sample), fp64, "
+                      f"{dt:.1f} s"}
+
+
+# ------------------------------------------------------------- our path ----
+def time_launches(fn, n, stream):
+    import torch
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(n):
+        fn(i)
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / 1e3
+
+
+def run_ours(args):
+    import torch
+
+    import head_attention_fwd_gb300 as attn
+    from head_attention_fwd_gb300 import _build
+    from head_attention_fwd_gb300.inputs import WORKLOADS, make_qkv
+
+    world, rank, local = dist_init(args.gpus)
+    _build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = WORKLOADS[args.workload]
+    stream = torch.cuda.current_stream()
+
+    # N_SETS independent input sets, generated on the device from fixed seeds.
+    g = torch.Generator(device=dev)
+    sets = []
+    for i in range(N_SETS):
+        g.manual_seed(w.seed * 100 + i + 1000 * rank)
+        q, k, v = (torch.randn(w.shape(), generator=g, device=dev, dtype=torch.float32).to(w.torch_dtype)
+                   for _ in range(3))
+        sets.append((q, k, v, torch.empty_like(q)))
+    set_bytes = sum(t.numel() * t.element_size() for t in sets[0])
+
+    def step(i):
+        q, k, v, o = sets[i % N_SETS]
+        attn.attn_fwd(q, k, v, o, layout=w.layout, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    rc, detail = attn.attn_get_device_status()
+    if rc:
+        raise RuntimeError(f"device status after warm-up: {attn.attn_status_string(rc)} ({detail:#x})")
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    barrier(world)
+    torch.cuda.synchronize()
+    t_local = time_launches(step, args.steps, stream)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    t = max_over_ranks(t_local, world)
+    rc, detail = attn.attn_get_device_status()
+    if rc:
+        raise RuntimeError(f"device status after timed region: {attn.attn_status_string(rc)}")
+
+    flops_step = w.attn_flops
+    value = flops_step * args.steps * world / t / 1e12
+    kernel_tflops = flops_step * args.steps / t_local / 1e12
+
+    if rank != 0:
+        barrier(world)
+        return
+
+    peaks = measured_peaks()
+    alg_bytes = 4 * w.B * w.h * w.S * w.d * torch.tensor([], dtype=w.torch_dtype).element_size()
+    khash = _build.source_hash()
+    roofline = {
+        "bound": "tensor", "achieved": kernel_tflops, "peak": peaks["bf16_tflops"], "unit": UNIT,
+        "frac": kernel_tflops / peaks["bf16_tflops"], "traffic": profile_traffic(khash),
+        "peak_source": f"{peaks['source']} dense bf16 burst (fp16 runs at the bf16 rate)",
+        "frac_of_sustained": kernel_tflops / peaks["bf16_tflops_sustained"],
+        "hbm_gbs_algorithmic": alg_bytes / (t_local / args.steps) / 1e9,
+        "hbm_frac": alg_bytes / (t_local / args.steps) / 1e9 / peaks["hbm_gbs"],
+        "alg_bytes_per_launch": alg_bytes, "flops_per_launch": flops_step,
+        "kernel_source_hash": khash,
+    }
+
+    # e2e through the public API with pinned host buffers.
+    qh, kh, vh = (t.cpu().pin_memory() for t in sets[0][:3])
+    oh = torch.empty_like(qh).pin_memory()
+    qd, kd, vd, od = (torch.empty_like(t) for t in sets[0])
+
+    def e2e_step(i):
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        attn.attn_fwd(qd, kd, vd, od, layout=w.layout, stream=stream)
+        oh.copy_(od, non_blocking=True)
+
+    n_e2e = max(20, min(args.steps, 500))
+    for i in range(5):
+        e2e_step(i)
+    t_e2e = time_launches(e2e_step, n_e2e, stream)
+    e2e = {"value": flops_step * n_e2e / t_e2e / 1e12, "unit": UNIT,
+           "h2d_bytes_per_step": 3 * qh.numel() * qh.element_size(),
+           "d2h_bytes_per_step": oh.numel() * oh.element_size()}
+
+    extra = {}
+    if not args.no_extra and world == 1:
+        extra = run_extra(attn, w, sets, stream, dev)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "h": w.h, "S": w.S, "d": w.d, "layout": "BHSD",
+                   "causal": False, "scale": w.scale, "global_batch": w.B * world,
+                   "parallelism": f"independent problem per rank x{world} (no collective)",
+                   "l2": f"{N_SETS} rotating input sets, {N_SETS * set_bytes / 2**20:.0f} MiB > 129 MB L2"},
+        "gpu_launches": args.steps,
+        "roofline": roofline,
+        "clocks": clocks,
+        "e2e": e2e,
+        "pct_of_tensor_peak": 100.0 * kernel_tflops / peaks["bf16_tflops"],
+    }
+    if world == 1 and not args.no_cpu:
+        from head_attention_fwd_gb300.inputs import make_qkv as mk
+        qc, kc, vc = mk(w)
+        line["cpu_baseline"] = cpu_baseline(w, qc, kc, vc)
+    if extra:
+        line["extra"] = extra
+    print(json.dumps(line), flush=True)
+    barrier(world)
+
+
+def run_extra(attn, w, sets, stream, dev):
+    """Unfused comparison on the same workload and fused throughput on the
+    other tensor-core workloads (each timed alone with CUDA events)."""
+    import torch
+    from head_attention_fwd_gb300.inputs import WORKLOADS
+
+    out = {}
+    q, k, v, o = sets[0]
+    ws = torch.empty(attn.attn_fwd_naive_workspace_bytes(w.B, w.h, w.S, q.dtype), dtype=torch.uint8,
+                     device=dev)
+    for _ in range(3):
+        attn.attn_fwd_naive(q, k, v, o, workspace=ws, layout=w.layout, stream=stream)
+    n = 20
+    t = time_launches(lambda i: attn.attn_fwd_naive(*sets[i % N_SETS], workspace=ws, layout=w.layout,
+                                                    stream=stream), n, stream)
+    out["naive_two_pass_" + w.name] = {"tflops": w.attn_flops * n / t / 1e12, "ms": t / n * 1e3,
+                                       "launches_per_call": 4}
+    del ws
+    for name in ("long_seq_bf16_peaky", "wide_head_bf16_bshd"):
+        ww = WORKLOADS[name]
+        g = torch.Generator(device=dev).manual_seed(ww.seed)
+        qq, kk, vv = (torch.randn(ww.shape(), generator=g, device=dev).to(ww.torch_dtype) for _ in range(3))
+        oo = torch.empty_like(qq)
+        lse = torch.empty((ww.B, ww.h, ww.S), dtype=torch.float32, device=dev) if ww.want_lse else None
+        for _ in range(3):
+            attn.attn_fwd(qq, kk, vv, oo, lse, layout=ww.layout, stream=stream)
+        n = 20
+        t = time_launches(lambda i: attn.attn_fwd(qq, kk, vv, oo, lse, layout=ww.layout, stream=stream),
+                          n, stream)
+        out[name] = {"tflops": ww.attn_flops * n / t / 1e12, "ms": t / n * 1e3}
+        del qq, kk, vv, oo, lse
+    wb = WORKLOADS["bert_base_qkv"]
+    g = torch.Generator(device=dev).manual_seed(wb.seed)
+    x = torch.randn((wb.B, wb.S, wb.D), generator=g, device=dev).to(wb.torch_dtype)
+    wq = (torch.randn((wb.D, 3 * wb.D), generator=g, device=dev) * wb.w_std).to(wb.torch_dtype)
+    oo = torch.empty((wb.B, wb.S, wb.h, wb.d), dtype=wb.torch_dtype, device=dev)
+    ws = torch.empty(attn.qkv_proj_attn_workspace_bytes(wb.B, wb.S, wb.D, x.dtype), dtype=torch.uint8,
+                     device=dev)
+    for _ in range(3):
+        attn.qkv_proj_attn(x, wq, wb.h, oo, ws, stream=stream)
+    n = 50
+    t = time_launches(lambda i: attn.qkv_proj_attn(x, wq, wb.h, oo, ws, stream=stream), n, stream)
+    fl = wb.attn_flops + wb.proj_flops
+    out["bert_base_qkv"] = {"tflops": fl / (t / n) / 1e12, "ms": t / n * 1e3,
+                            "flops": "projection 2*B*S*D*3D + attention 4*B*h*S^2*d"}
+    wc = WORKLOADS["single_head_f32"]
+    g = torch.Generator(device=dev).manual_seed(wc.seed)
+    qq, kk, vv = (torch.randn(wc.shape(), generator=g, device=dev) for _ in range(3))
+    oo = torch.empty_like(qq)
+    n = 200
+    t = time_launches(lambda i: attn.attn_fwd(qq, kk, vv, oo, stream=stream), n, stream)
+    out["single_head_f32"] = {"us": t / n * 1e6, "note": "latency-bound fp32 CUDA-core path"}
+    rc, detail = attn.attn_get_device_status()
+    if rc:
+        raise RuntimeError(f"device status after extra runs: {attn.attn_status_string(rc)}")
+    return out
+
+
+# ------------------------------------------------------- reference (CPU) ----
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from head_attention_fwd_gb300.inputs import WORKLOADS, make_qkv
+
+    oracle.build()
+    w = WORKLOADS[args.workload]
+    q, k, v = make_qkv(w)
+    cores = oracle.threads(0)
+    # size each step so that the whole run stays within about two minutes
+    dt, _, _ = oracle_rows_timing(w, q, k, v, max(cores, 32))
+    per_row = dt / max(cores, 32)
+    total_steps = args.steps + args.warmup
+    rows = int(max(cores, min(w.B * w.h * w.S, 120.0 / max(per_row, 1e-7) / max(total_steps, 1))))
+    for i in range(args.warmup):
+        oracle_rows_timing(w, q, k, v, rows, seed=100 + i)
+    t0 = time.perf_counter()
+    fl = 0.0
+    for i in range(args.steps):
+        _, f, _ = oracle_rows_timing(w, q, k, v, rows, seed=1000 + i)
+        fl += f
+    t = time.perf_counter() - t0
+    value = fl / t / 1e12
+    sample = f"{rows} of {w.B * w.h * w.S} query rows of {w.name} per step (seeded), fp64"
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t / max(args.steps, 1) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "h": w.h, "S": w.S, "d": w.d, "layout": "BHSD",
+                   "causal": False, "scale": w.scale},
+        "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle", "cores": cores, "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -10,6 +10,7 @@ Entry points (same names as the C ABI):
 * ``attn_fwd(q, k, v, ...)``        fused online-softmax attention
 * ``attn_fwd_naive(q, k, v, ...)``  unfused two-pass-softmax comparison path
 * ``qkv_proj_attn(x, w_qkv, h, ...)`` fused QKV projection, then attention
+* ``qkv_proj_attn_noalloc(x, w_qkv, h, ...)`` the same without a workspace argument
 * ``attn_get_device_status()``, ``attn_status_string(rc)``
 """
 
@@ -57,6 +58,8 @@ def lib() -> ctypes.CDLL:
             L.attn_fwd_naive_workspace_bytes.restype = sz
             L.qkv_proj_attn.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, vp, sz, vp]
             L.qkv_proj_attn.restype = ci
+            L.qkv_proj_attn_noalloc.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, vp]
+            L.qkv_proj_attn_noalloc.restype = ci
             L.qkv_proj_attn_workspace_bytes.argtypes = [ci, ci, ci, ci]
             L.qkv_proj_attn_workspace_bytes.restype = sz
             L.attn_status_string.argtypes = [ci]
@@ -180,6 +183,24 @@ def qkv_proj_attn(x, w_qkv, h: int, o=None, workspace=None, *, stream=None):
     if rc:
         raise AttnError(rc, "qkv_proj_attn")
     return o, workspace
+
+
+def qkv_proj_attn_noalloc(x, w_qkv, h: int, o=None, *, stream=None):
+    """qkv_proj_attn without a workspace argument, for callers that cannot allocate
+    device memory: the projection goes to the library's fixed static scratch
+    (ATTN_NOALLOC_SCRATCH_BYTES = 32 MiB per device).  The C call allocates nothing;
+    only the optional output below is allocated here, when ``o`` is not given.
+    Returns o [B,S,h,d]."""
+    torch = _torch()
+    B, S, D = (int(n) for n in x.shape)
+    if o is None:
+        o = torch.empty((B, S, h, D // h), dtype=x.dtype, device=x.device)
+    _check_dense(x, w_qkv, o)
+    rc = lib().qkv_proj_attn_noalloc(_ptr(x), _ptr(w_qkv), _ptr(o), B, S, D, h, dtype_code(x.dtype),
+                                     _stream_ptr(stream))
+    if rc:
+        raise AttnError(rc, "qkv_proj_attn_noalloc")
+    return o
 
 
 def attn_get_device_status(stream=None) -> tuple[int, int]:

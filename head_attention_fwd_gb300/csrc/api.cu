@@ -377,6 +377,8 @@ const char* attn_status_string(int status) {
     case ATTN_E_ALIAS: return "ATTN_E_ALIAS: output overlaps an input or the workspace";
     case ATTN_E_DEVICE: return "ATTN_E_DEVICE: no usable sm_103 device or driver entry point";
     case ATTN_E_TIMEOUT: return "ATTN_E_TIMEOUT: a kernel pipeline wait exceeded its limit";
+    case ATTN_E_SCRATCH_LIMIT:
+      return "ATTN_E_SCRATCH_LIMIT: problem exceeds the fixed scratch of qkv_proj_attn_noalloc";
     default: break;
   }
   if (status > 0) return cudaGetErrorString(static_cast<cudaError_t>(status));

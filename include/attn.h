@@ -14,7 +14,8 @@
  *  - All tensor pointers are DEVICE pointers owned by the caller.  The
  *    library keeps no reference to them after the call is enqueued and
  *    allocates no device memory of its own (it holds one 4-byte status word
- *    per device, a statically declared device variable).
+ *    per device and the fixed scratch of qkv_proj_attn_noalloc, both
+ *    statically declared device variables).
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *    default stream).  None of them synchronises, except
  *    attn_get_device_status.
@@ -61,7 +62,8 @@ enum {
   ATTN_E_WORKSPACE = -6, /* workspace NULL, misaligned or smaller than required        */
   ATTN_E_ALIAS = -7,     /* the output overlaps an input or the workspace              */
   ATTN_E_DEVICE = -8,    /* no usable sm_103 device / driver entry point missing       */
-  ATTN_E_TIMEOUT = -9    /* (device status only) a pipeline wait exceeded its limit    */
+  ATTN_E_TIMEOUT = -9,   /* (device status only) a pipeline wait exceeded its limit    */
+  ATTN_E_SCRATCH_LIMIT = -10 /* problem too large for qkv_proj_attn_noalloc's fixed scratch */
 };
 
 /*
@@ -129,6 +131,39 @@ int qkv_proj_attn(const void* x, const void* w_qkv, void* o, int B, int S, int D
                   void* workspace, size_t ws_bytes, void* stream);
 /* Workspace size for qkv_proj_attn: B·S·3D·elt bytes rounded up to 256; 0 when invalid. */
 size_t qkv_proj_attn_workspace_bytes(int B, int S, int D, int dtype);
+
+/*
+ * qkv_proj_attn_noalloc -- qkv_proj_attn for callers that cannot allocate
+ * device memory.  The pages have no counterpart to this entry point.
+ *
+ * Some callers cannot call cudaMalloc (or any allocator) at the point where
+ * they run attention: a plugin inside a host application that hands over only
+ * its input and output buffers and owns every other byte of device memory; a
+ * framework whose memory pool must account for all allocations; a
+ * latency-critical loop that cannot afford an allocation's implicit device
+ * synchronisation.  This entry point needs no workspace argument: the
+ * [B, S, 3D] projection goes to a fixed scratch array of
+ * ATTN_NOALLOC_SCRATCH_BYTES that the library declares statically in device
+ * memory (every GPU that loads the library holds it until the process exits).
+ * The call itself allocates nothing.
+ *
+ *   x, w_qkv, o, B, S, D, h, dtype, stream   as for qkv_proj_attn.
+ *
+ * Limit: B·S·3D·elt (rounded up to 256 bytes) must not exceed
+ * ATTN_NOALLOC_SCRATCH_BYTES (32 MiB, e.g. B·S <= 7281 at D = 768 in fp16);
+ * larger problems return ATTN_E_SCRATCH_LIMIT and launch nothing.
+ * The first call on each device resolves the scratch array's device address
+ * (with that device current), so make that first call before any stream
+ * capture.  All calls share the one array and it keeps the last call's
+ * contents; nothing in it needs to start at zero because the projection
+ * overwrites every element it later reads.  Calls that overlap on the GPU
+ * (for example on two streams at once) race on the array: serialise them.
+ * Errors: as qkv_proj_attn (without the workspace checks), plus
+ * ATTN_E_SCRATCH_LIMIT.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+int qkv_proj_attn_noalloc(const void* x, const void* w_qkv, void* o, int B, int S, int D, int h,
+                          int dtype, void* stream);
 
 /* Human-readable name of an ATTN_* status or a cudaError_t (positive). Never NULL. */
 const char* attn_status_string(int status);

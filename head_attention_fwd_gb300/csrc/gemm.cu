@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(192, 2)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_slot, 0);
   const WaitCtx wc{abort_flag, p.status, p.limit};
   const bool skip = *abort_flag != 0;
 
@@ -137,30 +137,28 @@ __global__ void __launch_bounds__(192, 2)
         mbar_wait_slow(bar(C::bar_full(kt % C::STAGES)), (kt / C::STAGES) & 1, drain, 0, false);
     }
   } else if (warp == 1) {
+    // The whole warp runs the issue loop; elect.sync inside the helpers picks
+    // the lane that issues, so the descriptors stay warp-uniform.
     constexpr uint32_t idesc = idesc_f16(128, BN, BF16, false, !BKMAJOR);
+    const uint64_t da = sdesc_sw128(sb, 16, 1024);
+    const uint64_t db = BKMAJOR ? sdesc_sw128(sb + C::A_BYTES, 16, 1024)
+                                : sdesc_sw128(sb + C::A_BYTES, C::B_CHUNK, 1024);
     bool ok = true;
     for (int kt = 0; kt < nk; ++kt) {
       const int s = kt % C::STAGES, u = kt / C::STAGES;
       ok = mbar_wait_warp(bar(C::bar_full(s)), u & 1, wc, gcode(ROLE_MMA, kt));
       if (!ok) break;
       tc_fence_after();
-      if (lane == 0) {
-        const uint32_t st = sb + s * C::STAGE;
+      const uint32_t st16 = (s * C::STAGE) >> 4;  // stage offset in descriptor address units
 #pragma unroll
-        for (int kk = 0; kk < C::BKE / 16; ++kk) {
-          const uint64_t a = sdesc_sw128(st + kk * 32, 16, 1024);
-          const uint64_t bd = BKMAJOR ? sdesc_sw128(st + C::A_BYTES + kk * 32, 16, 1024)
-                                      : sdesc_sw128(st + C::A_BYTES + kk * 2048, C::B_CHUNK, 1024);
-          mma_ss(tmem, a, bd, idesc, (kt > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(bar(C::bar_empty(s)));
+      for (int kk = 0; kk < C::BKE / 16; ++kk) {
+        const uint32_t ka = (kk * 32) >> 4, kb = (BKMAJOR ? kk * 32 : kk * 2048) >> 4;
+        mma_ss_elect(tmem, da + st16 + ka, db + st16 + kb, idesc, (kt > 0 || kk > 0) ? 1u : 0u);
       }
+      mma_commit_elect(bar(C::bar_empty(s)));
     }
-    if (lane == 0) mma_commit(bar(ok ? C::bar_acc() : C::bar_drain()));
-    if (!ok) {
-      const WaitCtx drain{abort_flag, p.status, p.limit};
-      mbar_wait_slow(bar(C::bar_drain()), 0, drain, 0, false);
-    }
+    mma_commit_elect(bar(ok ? C::bar_acc() : C::bar_drain()));
+    if (!ok) mbar_wait_slow(bar(C::bar_drain()), 0, wc, 0, false);
   } else {
     // -------------------------------------------------------- epilogue ----
     const uint32_t wq = warp & 3u;

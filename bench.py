@@ -85,13 +85,27 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """Maximum of a host float over all ranks (one all-reduce; host-side
+    timing only -- the attention itself has no collective)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cpu" if dist.get_backend() == "gloo" else "cuda"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def rank_seed(w, rank: int, set_index: int) -> int:
+    """Seed of input set `set_index` on `rank`: every rank draws its own problem."""
+    return w.seed * 100 + set_index + 1000 * rank
+
+
+def aggregate_tflops(flops_per_step: float, steps: int, world: int, t_max: float) -> float:
+    """Whole-job throughput: every rank ran `steps` steps of its own problem
+    (weak scaling), timed by the slowest rank."""
+    return flops_per_step * steps * world / t_max / 1e12
 
 
 # ---------------------------------------------------------------- clocks ----
@@ -226,7 +240,7 @@ def run_ours(args):
     g = torch.Generator(device=dev)
     sets = []
     for i in range(N_SETS):
-        g.manual_seed(w.seed * 100 + i + 1000 * rank)
+        g.manual_seed(rank_seed(w, rank, i))
         q, k, v = (torch.randn(w.shape(), generator=g, device=dev, dtype=torch.float32).to(w.torch_dtype)
                    for _ in range(3))
         sets.append((q, k, v, torch.empty_like(q)))
@@ -256,7 +270,7 @@ def run_ours(args):
         raise RuntimeError(f"device status after timed region: {attn.attn_status_string(rc)}")
 
     flops_step = w.attn_flops
-    value = flops_step * args.steps * world / t / 1e12
+    value = aggregate_tflops(flops_step, args.steps, world, t)
     kernel_tflops = flops_step * args.steps / t_local / 1e12
 
     if rank != 0:

@@ -66,6 +66,8 @@ def lib() -> ctypes.CDLL:
             L.attn_status_string.restype = ctypes.c_char_p
             L.attn_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
             L.attn_get_device_status.restype = ci
+            L.attn_selftest_wait_timeout.argtypes = [ctypes.c_longlong, vp]
+            L.attn_selftest_wait_timeout.restype = ci
             L.attn_abi_version.argtypes = []
             L.attn_abi_version.restype = ci
             _lib = L
@@ -201,6 +203,14 @@ def qkv_proj_attn_noalloc(x, w_qkv, h: int, o=None, *, stream=None):
     if rc:
         raise AttnError(rc, "qkv_proj_attn_noalloc")
     return o
+
+
+def attn_selftest_wait_timeout(limit_cycles: int, stream=None) -> None:
+    """Launch the stalled-wait self-test (see include/attn.h); read the result
+    with attn_get_device_status()."""
+    rc = lib().attn_selftest_wait_timeout(int(limit_cycles), _stream_ptr(stream))
+    if rc:
+        raise AttnError(rc, "attn_selftest_wait_timeout")
 
 
 def attn_get_device_status(stream=None) -> tuple[int, int]:

@@ -11,6 +11,7 @@
 
 #include "attn.h"
 #include "common.h"
+#include "ptx.cuh"
 
 namespace {
 
@@ -130,6 +131,23 @@ int make_matrix_map(CUtensorMap* m, const void* base, int dtype, long long Z1, l
 }
 
 int to_rc(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : static_cast<int>(e); }
+
+// One warp waits on an mbarrier that nothing will ever arrive on, with the
+// same bounded wait the pipeline kernels use; it must give up after `limit`
+// cycles, record the code in the status word and return.
+__global__ void selftest_wait_kernel(unsigned* status, long long limit) {
+  __shared__ __align__(8) uint64_t mbar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    attn::mbar_init(attn::smem_u32(&mbar), 1);
+    abort_flag = 0;
+    attn::fence_mbar_init();
+  }
+  __syncthreads();
+  const attn::WaitCtx wc{&abort_flag, status, limit};
+  const uint32_t code = (attn::KID_SELFTEST << 24) | (attn::ROLE_LOAD << 16);
+  attn::mbar_wait_warp(attn::smem_u32(&mbar), 0, wc, code);
+}
 
 // Checks shared by attn_fwd and attn_fwd_naive.  Makes no CUDA call.
 int validate_attn(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -383,6 +401,15 @@ const char* attn_status_string(int status) {
   }
   if (status > 0) return cudaGetErrorString(static_cast<cudaError_t>(status));
   return "unknown attn status";
+}
+
+int attn_selftest_wait_timeout(long long limit_cycles, void* stream) {
+  if (limit_cycles < 1 || limit_cycles > 10000000000LL) return ATTN_E_SHAPE;
+  DeviceState* ds = nullptr;
+  int rc = device_setup(&ds);
+  if (rc) return rc;
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(ds->status, limit_cycles);
+  return to_rc(cudaGetLastError());
 }
 
 int attn_get_device_status(void* stream, unsigned int* detail) {

@@ -11,7 +11,7 @@
 namespace attn {
 
 // Device status word codes (kernel id << 24 | role << 16 | tile index).
-enum KernelId : uint32_t { KID_FLASH = 1, KID_GEMM = 2, KID_SIMT = 3, KID_NAIVE = 4 };
+enum KernelId : uint32_t { KID_FLASH = 1, KID_GEMM = 2, KID_SIMT = 3, KID_NAIVE = 4, KID_SELFTEST = 15 };
 enum RoleId : uint32_t { ROLE_LOAD = 1, ROLE_MMA = 2, ROLE_SOFTMAX = 3, ROLE_EPILOGUE = 4 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

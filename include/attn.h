@@ -178,6 +178,19 @@ const char* attn_status_string(int status);
  */
 int attn_get_device_status(void* stream, unsigned int* detail);
 
+/*
+ * attn_selftest_wait_timeout -- diagnostics for the failure reporting above.
+ * The pages have no counterpart; this exercises the library's own handling
+ * of a stalled pipeline.  Launches one warp that waits on an mbarrier nothing
+ * will ever arrive on, with the same bounded wait the attention kernels use
+ * and a limit of `limit_cycles` SM clock cycles (1 .. 10^10).  The kernel
+ * gives up after the limit, records detail code 15 << 24 | 1 << 16 in the
+ * device status word and returns: attn_get_device_status then reports
+ * ATTN_E_TIMEOUT, and the CUDA context stays usable.  No fault, trap or hang
+ * is involved.  Errors: ATTN_E_SHAPE for a limit out of range, ATTN_E_DEVICE.
+ */
+int attn_selftest_wait_timeout(long long limit_cycles, void* stream);
+
 /* ABI version of this header: 1. */
 int attn_abi_version(void);
 

@@ -25,6 +25,8 @@ LAYOUT_BSHD = 1  # head-interleaved [B, S, h, d]
 ATTN_F32, ATTN_F16, ATTN_BF16 = 0, 1, 2
 ATTN_OK = 0
 ATTN_E_TIMEOUT = -9
+ATTN_E_MISMATCH = -11
+ATTN_KERNEL_NAIVE, ATTN_KERNEL_ONLINE = 0, 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libattn_gb300.so")
@@ -68,6 +70,13 @@ def lib() -> ctypes.CDLL:
             L.attn_get_device_status.restype = ci
             L.attn_selftest_wait_timeout.argtypes = [ctypes.c_longlong, vp]
             L.attn_selftest_wait_timeout.restype = ci
+            L.attn_select_kernel.argtypes = [ci, ci, ci]
+            L.attn_select_kernel.restype = ci
+            L.attn_fwd_auto.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, cf, ci, ci, ci, ci, vp, sz, vp,
+                                        ctypes.POINTER(ci)]
+            L.attn_fwd_auto.restype = ci
+            L.attn_compare.argtypes = [vp, vp, ctypes.c_longlong, ci, cf, ctypes.POINTER(cf), vp]
+            L.attn_compare.restype = ci
             L.attn_abi_version.argtypes = []
             L.attn_abi_version.restype = ci
             _lib = L
@@ -203,6 +212,56 @@ def qkv_proj_attn_noalloc(x, w_qkv, h: int, o=None, *, stream=None):
     if rc:
         raise AttnError(rc, "qkv_proj_attn_noalloc")
     return o
+
+
+def select_kernel(option_enabled: bool, seq_len: int, threshold: int = 0) -> int:
+    """ATTN_KERNEL_ONLINE when the option is on and seq_len > threshold (1024 by default)."""
+    return int(lib().attn_select_kernel(int(bool(option_enabled)), int(seq_len), int(threshold)))
+
+
+def attn_fwd_auto(q, k, v, o=None, lse=None, workspace=None, *, option_enabled: bool = True,
+                  threshold: int = 0, layout: int = LAYOUT_BHSD, scale: float | None = None,
+                  want_lse: bool = False, stream=None):
+    """attn_fwd or attn_fwd_naive as select_kernel picks.  Returns (o, lse or None, kernel)."""
+    torch = _torch()
+    B, h, S, d = _dims(q, layout)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, h, S), dtype=torch.float32, device=q.device)
+    if workspace is None and select_kernel(option_enabled, S, threshold) == ATTN_KERNEL_NAIVE:
+        workspace = torch.empty(attn_fwd_naive_workspace_bytes(B, h, S, q.dtype), dtype=torch.uint8,
+                                device=q.device)
+    _check_dense(q, k, v, o, lse, workspace)
+    chosen = ctypes.c_int(-1)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().attn_fwd_auto(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, h, S, d,
+                             float(scale) if scale else 0.0, layout, dtype_code(q.dtype),
+                             int(bool(option_enabled)), int(threshold), _ptr(workspace), nbytes,
+                             _stream_ptr(stream), ctypes.byref(chosen))
+    if rc:
+        raise AttnError(rc, "attn_fwd_auto")
+    return o, lse, chosen.value
+
+
+def attn_compare(a, b, atol: float, stream=None) -> tuple[int, float]:
+    """(status, max |a - b|) of two device tensors of one dtype (synchronises the stream)."""
+    if a.shape != b.shape or a.dtype != b.dtype:
+        raise ValueError("a and b must share shape and dtype")
+    _check_dense(a, b)
+    mx = ctypes.c_float(0.0)
+    rc = lib().attn_compare(_ptr(a), _ptr(b), a.numel(), dtype_code(a.dtype), float(atol),
+                            ctypes.byref(mx), _stream_ptr(stream))
+    return int(rc), float(mx.value)
+
+
+def assert_numerically_equal(out_naive, out_online, atol: float = 1e-3, stream=None) -> None:
+    """Raises AssertionError when the two outputs differ by more than atol."""
+    rc, mx = attn_compare(out_naive, out_online, atol, stream)
+    if rc == ATTN_E_MISMATCH:
+        raise AssertionError(f"online softmax disagrees with naive: max |diff| {mx:.3e} > {atol}")
+    if rc:
+        raise AttnError(rc, "attn_compare")
 
 
 def attn_selftest_wait_timeout(limit_cycles: int, stream=None) -> None:

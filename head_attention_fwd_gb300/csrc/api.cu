@@ -395,12 +395,48 @@ const char* attn_status_string(int status) {
     case ATTN_E_ALIAS: return "ATTN_E_ALIAS: output overlaps an input or the workspace";
     case ATTN_E_DEVICE: return "ATTN_E_DEVICE: no usable sm_103 device or driver entry point";
     case ATTN_E_TIMEOUT: return "ATTN_E_TIMEOUT: a kernel pipeline wait exceeded its limit";
+    case ATTN_E_MISMATCH: return "ATTN_E_MISMATCH: the two outputs differ by more than atol";
     case ATTN_E_SCRATCH_LIMIT:
       return "ATTN_E_SCRATCH_LIMIT: problem exceeds the fixed scratch of qkv_proj_attn_noalloc";
     default: break;
   }
   if (status > 0) return cudaGetErrorString(static_cast<cudaError_t>(status));
   return "unknown attn status";
+}
+
+int attn_select_kernel(int option_enabled, int seq_len, int threshold) {
+  const int thr = threshold > 0 ? threshold : 1024;
+  return (option_enabled && seq_len > thr) ? ATTN_KERNEL_ONLINE : ATTN_KERNEL_NAIVE;
+}
+
+int attn_fwd_auto(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h,
+                  int S, int d, float scale, int layout, int dtype, int option_enabled,
+                  int threshold, void* workspace, size_t ws_bytes, void* stream, int* chosen) {
+  const int kind = attn_select_kernel(option_enabled, S, threshold);
+  if (chosen) *chosen = kind;
+  if (kind == ATTN_KERNEL_ONLINE)
+    return attn_fwd(q, k, v, o, lse, B, h, S, d, scale, layout, dtype, stream);
+  return attn_fwd_naive(q, k, v, o, lse, B, h, S, d, scale, layout, dtype, workspace, ws_bytes,
+                        stream);
+}
+
+int attn_compare(const void* a, const void* b, long long n, int dtype, float atol, float* max_abs,
+                 void* stream) {
+  if (max_abs) *max_abs = 0.f;
+  if (!a || !b) return ATTN_E_NULL;
+  if (dtype != ATTN_F32 && dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_E_DTYPE;
+  if (n < 0 || !(atol >= 0.f)) return ATTN_E_SHAPE;
+  DeviceState* ds = nullptr;
+  int rc = device_setup(&ds);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float result = 0.f;
+  if (n > 0) {
+    rc = to_rc(attn::launch_max_abs_diff(a, b, n, dtype, &result, st));
+    if (rc) return rc;
+  }
+  if (max_abs) *max_abs = result;
+  return (result <= atol) ? ATTN_OK : ATTN_E_MISMATCH;
 }
 
 int attn_selftest_wait_timeout(long long limit_cycles, void* stream) {

@@ -74,4 +74,10 @@ struct NaiveSoftmaxLaunch {
 };
 cudaError_t launch_naive_softmax(const NaiveSoftmaxLaunch& a, cudaStream_t st);
 
+// max |a - b| over n elements of two device buffers (dtype as attn.h);
+// synchronises the stream and writes the result to *host_max.  Uses one
+// statically declared device word: concurrent calls on different streams race.
+cudaError_t launch_max_abs_diff(const void* a, const void* b, long long n, int dtype,
+                                float* host_max, cudaStream_t st);
+
 }  // namespace attn

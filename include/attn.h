@@ -63,8 +63,11 @@ enum {
   ATTN_E_ALIAS = -7,     /* the output overlaps an input or the workspace              */
   ATTN_E_DEVICE = -8,    /* no usable sm_103 device / driver entry point missing       */
   ATTN_E_TIMEOUT = -9,   /* (device status only) a pipeline wait exceeded its limit    */
-  ATTN_E_SCRATCH_LIMIT = -10 /* problem too large for qkv_proj_attn_noalloc's fixed scratch */
+  ATTN_E_SCRATCH_LIMIT = -10, /* problem too large for qkv_proj_attn_noalloc's fixed scratch */
+  ATTN_E_MISMATCH = -11  /* attn_compare: the two outputs differ by more than atol     */
 };
+
+typedef enum { ATTN_KERNEL_NAIVE = 0, ATTN_KERNEL_ONLINE = 1 } attn_kernel;
 
 /*
  * attn_fwd -- fused attention forward (online softmax, one kernel launch).
@@ -164,6 +167,38 @@ size_t qkv_proj_attn_workspace_bytes(int B, int S, int D, int dtype);
 #define ATTN_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 int qkv_proj_attn_noalloc(const void* x, const void* w_qkv, void* o, int B, int S, int D, int h,
                           int dtype, void* stream);
+
+/*
+ * attn_select_kernel -- the softmax-strategy policy of the online-softmax
+ * proposal page ("[WebGPU] Proposal: Add an option to use online softmax
+ * instead of naive softmax", §六 select_kernel): the online (fused) kernel
+ * when the option is enabled and seq_len exceeds the threshold, the naive
+ * two-pass kernel otherwise.  threshold <= 0 selects the page's 1024.
+ * Returns ATTN_KERNEL_ONLINE or ATTN_KERNEL_NAIVE.  Host only; no CUDA call.
+ */
+int attn_select_kernel(int option_enabled, int seq_len, int threshold);
+
+/*
+ * attn_fwd_auto -- attn_fwd or attn_fwd_naive, as attn_select_kernel picks
+ * for (option_enabled, S, threshold).  Arguments as attn_fwd; `workspace` /
+ * `ws_bytes` are needed only when the naive kernel is picked (size from
+ * attn_fwd_naive_workspace_bytes; ATTN_E_WORKSPACE otherwise).  `chosen`
+ * (may be NULL) receives the attn_kernel that ran.
+ */
+int attn_fwd_auto(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h,
+                  int S, int d, float scale, int layout, int dtype, int option_enabled,
+                  int threshold, void* workspace, size_t ws_bytes, void* stream, int* chosen);
+
+/*
+ * attn_compare -- the numeric-agreement guard of the same page (§六
+ * assert_numerically_equal): synchronises `stream`, then compares n elements
+ * of two device buffers of `dtype` and writes max |a - b| to *max_abs
+ * (host, may be NULL).  Returns ATTN_OK when it is <= atol, ATTN_E_MISMATCH
+ * otherwise (a NaN counts as a mismatch), or an error.  The page uses
+ * atol = 1e-3; for 16-bit outputs the two kernels also round P differently.
+ */
+int attn_compare(const void* a, const void* b, long long n, int dtype, float atol, float* max_abs,
+                 void* stream);
 
 /* Human-readable name of an ATTN_* status or a cudaError_t (positive). Never NULL. */
 const char* attn_status_string(int status);

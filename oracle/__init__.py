@@ -16,6 +16,7 @@ Every function follows a passage of the pages (page title, section):
 * ``attention``, ``attention_rows`` -- ch.2 §2.2-§2.4 (scores, softmax, weighted sum);
                                  layouts from the WebGPU page §QKV 矩阵的内存合并模式选择
 * ``qkv_projection``, ``split_heads``, ``qkv_proj_attention`` -- ch.2 §2.1 (fused [D,3D] weight)
+* ``attention_grouped``       -- the "split" (head-group) layout of the same WebGPU section
 * ``decode``                  -- IEEE-754 binary16 / bfloat16 widening of the GPU's input bytes
 
 The pins that tie each function to the pages and to mathematics (not to
@@ -81,6 +82,8 @@ def bind(lib):
                                        _c_double_p, _c_double_p]
     lib.oracle_qkv_proj_attention.argtypes = [vp, vp, cint, i64, i64, i64, i64, dbl,
                                               _c_double_p, _c_double_p, cint]
+    lib.oracle_attention_grouped.argtypes = [vp, vp, vp, cint, i64, i64, i64, i64, i64, dbl,
+                                             _c_double_p, _c_double_p, cint]
     return lib
 
 
@@ -236,4 +239,20 @@ def qkv_proj_attention(x, w, h: int, scale: float | None = None, nthreads: int =
     if _load().oracle_qkv_proj_attention(xa.ctypes.data, wa.ctypes.data, et, B, S, D, h, scale,
                                          _dp(o), _dp(lse), nthreads):
         raise ValueError("oracle_qkv_proj_attention: bad arguments")
+    return o, lse
+
+
+def attention_grouped(q, k, v, hg: int, scale: float | None = None, nthreads: int = 0):
+    """Attention on the head-group layout [B, H/hg, S, hg, d]: (o same layout, lse [B,H,S])."""
+    B, G, S, hg_, d = (int(n) for n in q.shape)
+    if hg_ != hg or tuple(k.shape) != tuple(q.shape) or tuple(v.shape) != tuple(q.shape):
+        raise ValueError("q, k, v must be [B, H/hg, S, hg, d]")
+    H = G * hg
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    (qa, et), (ka, _), (va, _) = _raw(q), _raw(k), _raw(v)
+    o = np.empty(tuple(q.shape), dtype=np.float64)
+    lse = np.empty((B, H, S), dtype=np.float64)
+    if _load().oracle_attention_grouped(qa.ctypes.data, ka.ctypes.data, va.ctypes.data, et, B, H, S,
+                                        d, hg, scale, _dp(o), _dp(lse), nthreads):
+        raise ValueError("oracle_attention_grouped: bad arguments")
     return o, lse

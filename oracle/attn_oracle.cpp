@@ -101,6 +101,17 @@ void layout_strides(int layout, int64_t H, int64_t S, int64_t d, int64_t rs,
   }
 }
 
+// The third layout of the same section ("split", head groups): the heads
+// form groups of hg; each group's data is stored contiguously, positions
+// first, the group's heads interleaved within a position:
+//   [B, H/hg, S, hg, d].
+// Element (b, h, s, e) sits at
+//   b*H*S*d + (h / hg)*S*hg*d + s*hg*d + (h % hg)*d + e.
+int64_t grouped_index(int64_t H, int64_t S, int64_t d, int64_t hg, int64_t b, int64_t h, int64_t s,
+                      int64_t e) {
+  return b * H * S * d + (h / hg) * S * hg * d + s * hg * d + (h % hg) * d + e;
+}
+
 // [T2] §2.3: the three-step numerically stable softmax of one row.
 //   step 1  m = max_i s_i
 //   step 2  d = sum_i exp(s_i - m)
@@ -326,6 +337,39 @@ int oracle_qkv_proj_attention(const void* x, const void* w, int et, int64_t B, i
   oracle_split_heads(qkv.data(), B, S, D, H, q.data(), k.data(), v.data());
   return oracle_attention(q.data(), k.data(), v.data(), ET_F64, B, H, S, d, 1, scale, o, lse,
                           nthreads);
+}
+
+// Attention over the grouped layout: q, k, v, o are [B, H/hg, S, hg, d]
+// (see grouped_index), lse is [B, H, S].  Same arithmetic as
+// oracle_attention; only the addressing differs.
+int oracle_attention_grouped(const void* q, const void* k, const void* v, int et, int64_t B,
+                             int64_t H, int64_t S, int64_t d, int64_t hg, double scale, double* o,
+                             double* lse, int nthreads) {
+  if (!q || !k || !v || !o || B < 1 || H < 1 || S < 1 || d < 1 || hg < 1 || H % hg || et < 0 ||
+      et > 3)
+    return -1;
+  parallel_rows(B * H * S, nthreads, [&](int64_t r) {
+    thread_local std::vector<double> score, prob;
+    score.resize(S);
+    prob.resize(S);
+    const int64_t b = r / (H * S), h = (r / S) % H, i = r % S;
+    for (int64_t j = 0; j < S; ++j) {
+      double dot = 0.0;
+      for (int64_t e = 0; e < d; ++e)
+        dot += load_elem(q, et, grouped_index(H, S, d, hg, b, h, i, e)) *
+               load_elem(k, et, grouped_index(H, S, d, hg, b, h, j, e));
+      score[j] = dot * scale;
+    }
+    double m = 0.0, l = 0.0;
+    softmax_three_step(score.data(), S, prob.data(), &m, &l);
+    for (int64_t e = 0; e < d; ++e) {
+      double acc = 0.0;
+      for (int64_t j = 0; j < S; ++j) acc += prob[j] * load_elem(v, et, grouped_index(H, S, d, hg, b, h, j, e));
+      o[grouped_index(H, S, d, hg, b, h, i, e)] = acc;
+    }
+    if (lse) lse[r] = m + std::log(l);
+  });
+  return 0;
 }
 
 }  // extern "C"

@@ -323,3 +323,33 @@ def test_bad_arguments_are_rejected():
         oracle.attention(q, q, np.zeros((1, 1, 5, 4)))
     with pytest.raises(ValueError):
         oracle.attention_rows(q, q, q, [4])
+
+
+# ------------------------------------------------------- grouped layout ----
+def _to_grouped(a, hg):
+    """[B,H,S,d] -> [B,H/hg,S,hg,d] by numpy reshape/transpose (the layout's definition)."""
+    B, H, S, d = a.shape
+    return np.ascontiguousarray(a.reshape(B, H // hg, hg, S, d).transpose(0, 1, 3, 2, 4))
+
+
+@pytest.mark.parametrize("H,hg", [(4, 1), (4, 2), (4, 4), (6, 3)])
+def test_grouped_layout_matches_contiguous(H, hg):
+    B, S, d = 2, 11, 8
+    q, k, v = (RNG.standard_normal((B, H, S, d)) for _ in range(3))
+    o0, l0 = oracle.attention(q, k, v, layout=0)
+    og, lg = oracle.attention_grouped(_to_grouped(q, hg), _to_grouped(k, hg), _to_grouped(v, hg), hg)
+    np.testing.assert_array_equal(og, _to_grouped(o0, hg))
+    np.testing.assert_array_equal(lg, l0)
+
+
+def test_grouped_extremes_are_the_other_two_layouts():
+    """hg = 1 is the contiguous layout byte for byte; hg = H the head-interleaved one."""
+    B, H, S, d = 1, 3, 7, 4
+    q, k, v = (RNG.standard_normal((B, H, S, d)) for _ in range(3))
+    o1, _ = oracle.attention_grouped(q.reshape(B, H, S, 1, d), k.reshape(B, H, S, 1, d),
+                                     v.reshape(B, H, S, 1, d), 1)
+    np.testing.assert_array_equal(o1.reshape(B, H, S, d), oracle.attention(q, k, v, layout=0)[0])
+    t = lambda a: np.ascontiguousarray(a.transpose(0, 2, 1, 3))
+    oH, _ = oracle.attention_grouped(t(q).reshape(B, 1, S, H, d), t(k).reshape(B, 1, S, H, d),
+                                     t(v).reshape(B, 1, S, H, d), H)
+    np.testing.assert_array_equal(oH.reshape(B, S, H, d), oracle.attention(t(q), t(k), t(v), layout=1)[0])

@@ -29,6 +29,8 @@ MUTANTS = {
     "layout strides swapped": ("*sh = d;\n    *ss = rs;", "*sh = rs;\n    *ss = d;"),
     "split: head from wrong index": ("head = (c % D) / d, e = c % d;", "head = (c % d) % H, e = c % d;"),
     "f16 exponent bias off": ("expo - 15", "expo - 14"),
+    # (mutants must keep every index in bounds: they run inside the test process)
+    "grouped: group stride too small": ("(h / hg) * S * hg * d + s * hg * d", "(h / hg) * S * d + s * hg * d"),
     "projection transposed weight": ("wd[i] = load_elem(w, et, i);",
                                      "wd[i] = load_elem(w, et, (i % N) * D + i / N);"),
 }

@@ -22,6 +22,7 @@ import threading
 
 LAYOUT_BHSD = 0  # contiguous [B, h, S, d]
 LAYOUT_BSHD = 1  # head-interleaved [B, S, h, d]
+LAYOUT_GROUPED = 2  # head groups [B, h/hg, S, hg, d] (attn_fwd_grouped)
 ATTN_F32, ATTN_F16, ATTN_BF16 = 0, 1, 2
 ATTN_OK = 0
 ATTN_E_TIMEOUT = -9
@@ -54,6 +55,8 @@ def lib() -> ctypes.CDLL:
             vp, ci, cf, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
             L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, cf, ci, ci, vp]
             L.attn_fwd.restype = ci
+            L.attn_fwd_grouped.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp]
+            L.attn_fwd_grouped.restype = ci
             L.attn_fwd_naive.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, cf, ci, ci, vp, sz, vp]
             L.attn_fwd_naive.restype = ci
             L.attn_fwd_naive_workspace_bytes.argtypes = [ci, ci, ci, ci]
@@ -145,6 +148,28 @@ def attn_fwd(q, k, v, o=None, lse=None, *, layout: int = LAYOUT_BHSD, scale: flo
                         float(scale) if scale else 0.0, layout, dtype_code(q.dtype), _stream_ptr(stream))
     if rc:
         raise AttnError(rc, "attn_fwd")
+    return o, lse
+
+
+def attn_fwd_grouped(q, k, v, o=None, lse=None, *, scale: float | None = None, want_lse: bool = False,
+                     stream=None):
+    """attn_fwd on the head-group layout: q, k, v are [B, h/hg, S, hg, d].  Returns (o, lse or None)."""
+    torch = _torch()
+    if q.dim() != 5:
+        raise ValueError("q must be [B, h/hg, S, hg, d]")
+    B, G, S, hg, d = (int(n) for n in q.shape)
+    h = G * hg
+    if k.shape != q.shape or v.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share shape and dtype")
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, h, S), dtype=torch.float32, device=q.device)
+    _check_dense(q, k, v, o, lse)
+    rc = lib().attn_fwd_grouped(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, h, S, d, hg,
+                                float(scale) if scale else 0.0, dtype_code(q.dtype), _stream_ptr(stream))
+    if rc:
+        raise AttnError(rc, "attn_fwd_grouped")
     return o, lse
 
 

@@ -130,6 +130,24 @@ int make_matrix_map(CUtensorMap* m, const void* base, int dtype, long long Z1, l
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_E_DEVICE;
 }
 
+// Tensor map of the attention kernel over one of Q, K, V: dims
+// (d, hg, S, (H/hg)·B) with element strides sh (head within the group), ss
+// (position) and sg (group; the batch stride must equal (H/hg)·sg).
+int make_flash_map(CUtensorMap* m, const void* base, int dtype, long long B, long long H, long long S,
+                   long long d, long long hg, long long sh, long long ss, long long sg) {
+  const cuuint64_t e = static_cast<cuuint64_t>(elt_bytes(dtype));
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hg),
+                        static_cast<cuuint64_t>(S), static_cast<cuuint64_t>((H / hg) * B)};
+  cuuint64_t strides[3] = {sh * e, ss * e, sg * e};
+  cuuint32_t box[4] = {64, 1, 128, 1}, estr[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType dt =
+      dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUresult r = g_encode(m, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_E_DEVICE;
+}
+
 int to_rc(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : static_cast<int>(e); }
 
 // One warp waits on an mbarrier that nothing will ever arrive on, with the
@@ -188,21 +206,36 @@ void o_strides(int layout, long long H, long long S, long long d, long long rs, 
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Flash launch on tensors of a [B,H,S,d] problem with row stride rs (layout 1).
+// Element strides of a [B,H,S,d] problem seen as heads in groups of hg
+// (see make_flash_map): layout 0 -> hg = 1, layout 1 -> hg = H with row
+// stride rs, layout 2 (head groups) -> the given hg.
+struct GroupedStrides {
+  long long hg, sb, sg, sh, ss;
+};
+GroupedStrides grouped_strides(int layout, long long H, long long S, long long d, long long rs,
+                               long long hg) {
+  if (layout == ATTN_LAYOUT_BHSD) return {1, H * S * d, S * d, d, d};
+  if (layout == ATTN_LAYOUT_BSHD) return {H, S * rs, S * rs, d, rs};
+  return {hg, H * S * d, S * hg * d, d, hg * d};
+}
+
+// Flash launch on tensors of a [B,H,S,d] problem; inputs and output may have
+// different row strides (rs_in, rs_out: layout 1 only).
 int run_flash(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h, int S,
-              int d, float scale, int layout, int dtype, long long rs_in, long long rs_out,
-              unsigned* status, cudaStream_t st) {
+              int d, float scale, int layout, long long hg, int dtype, long long rs_in,
+              long long rs_out, unsigned* status, cudaStream_t st) {
   attn::FlashLaunch a;
-  int swap = 0;
-  int rc = make_map(&a.tq, q, dtype, layout, B, h, S, d, rs_in, 128, &swap);
-  if (!rc) rc = make_map(&a.tk, k, dtype, layout, B, h, S, d, rs_in, 128, &swap);
-  if (!rc) rc = make_map(&a.tv, v, dtype, layout, B, h, S, d, rs_in, 128, &swap);
+  const GroupedStrides gi = grouped_strides(layout, h, S, d, rs_in, hg);
+  int rc = make_flash_map(&a.tq, q, dtype, B, h, S, d, gi.hg, gi.sh, gi.ss, gi.sg);
+  if (!rc) rc = make_flash_map(&a.tk, k, dtype, B, h, S, d, gi.hg, gi.sh, gi.ss, gi.sg);
+  if (!rc) rc = make_flash_map(&a.tv, v, dtype, B, h, S, d, gi.hg, gi.sh, gi.ss, gi.sg);
   if (rc) return rc;
+  const GroupedStrides go = grouped_strides(layout, h, S, d, rs_out, hg);
   a.o = o;
   a.lse = lse;
-  o_strides(layout, h, S, d, rs_out, &a.o_sb, &a.o_sh, &a.o_ss);
+  a.o_sb = go.sb, a.o_sg = go.sg, a.o_sh = go.sh, a.o_ss = go.ss;
   a.B = B, a.H = h, a.S = S, a.d = d;
-  a.hs_swap = swap;
+  a.hg = static_cast<int>(gi.hg);
   a.bf16 = dtype == ATTN_BF16;
   a.scale = scale;
   a.status = status;
@@ -237,7 +270,21 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
     return to_rc(attn::launch_simt_fwd(a, st));
   }
   const long long rs = static_cast<long long>(h) * d;
-  return run_flash(q, k, v, o, lse, B, h, S, d, sc, layout, dtype, rs, rs, ds->status, st);
+  return run_flash(q, k, v, o, lse, B, h, S, d, sc, layout, 1, dtype, rs, rs, ds->status, st);
+}
+
+int attn_fwd_grouped(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h,
+                     int S, int d, int heads_per_group, float scale, int dtype, void* stream) {
+  int rc = validate_attn(q, k, v, o, lse, B, h, S, d, ATTN_LAYOUT_BHSD, dtype);
+  if (rc) return rc;
+  if (dtype == ATTN_F32) return ATTN_E_DTYPE;
+  if (heads_per_group < 1 || h % heads_per_group) return ATTN_E_SHAPE;
+  DeviceState* ds = nullptr;
+  if ((rc = device_setup(&ds))) return rc;
+  const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(d));
+  const long long rs = static_cast<long long>(h) * d;
+  return run_flash(q, k, v, o, lse, B, h, S, d, sc, ATTN_LAYOUT_GROUPED, heads_per_group, dtype, rs,
+                   rs, ds->status, static_cast<cudaStream_t>(stream));
 }
 
 size_t attn_fwd_naive_workspace_bytes(int B, int h, int S, int dtype) {
@@ -379,8 +426,8 @@ int qkv_proj_attn(const void* x, const void* w_qkv, void* o, int B, int S, int D
   //    blocks of each row, i.e. head-interleaved with row stride 3D.
   const uint8_t* base = static_cast<const uint8_t*>(workspace);
   return run_flash(base, base + static_cast<size_t>(D) * 2, base + static_cast<size_t>(2 * D) * 2, o,
-                   nullptr, B, h, S, d, 1.0f / sqrtf(static_cast<float>(d)), ATTN_LAYOUT_BSHD, dtype,
-                   3LL * D, D, ds->status, st);
+                   nullptr, B, h, S, d, 1.0f / sqrtf(static_cast<float>(d)), ATTN_LAYOUT_BSHD, 1,
+                   dtype, 3LL * D, D, ds->status, st);
 }
 
 const char* attn_status_string(int status) {

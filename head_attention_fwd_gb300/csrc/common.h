@@ -7,18 +7,19 @@
 
 namespace attn {
 
-// Tensor-map dimension order for a [B, H, S, d] problem:
-//   hs_swap = 0: dims (d, S, H, B)  -- contiguous layout [B,H,S,d]
-//   hs_swap = 1: dims (d, H, S, B)  -- head-interleaved layout [B,S,H,d]
-// so that the byte strides always grow with the dimension index.
+// Tensor maps of the attention kernel: every layout is seen as heads in
+// groups of hg, dims (d, hg, S, (H/hg)·B) -- feature, head within the group,
+// position, then group and batch merged (the batch stride is always H/hg
+// group strides).  Contiguous [B,H,S,d] is hg = 1, head-interleaved
+// [B,S,H,d] is hg = H, and the head-group layout [B,H/hg,S,hg,d] is general.
 
 struct FlashLaunch {
-  CUtensorMap tq, tk, tv;       // 4-d maps, box = 64 features x 128 rows
+  CUtensorMap tq, tk, tv;       // 4-d maps, box = 64 features x 1 x 128 positions x 1
   void* o;                      // output, element strides below (feature stride 1)
   float* lse;                   // [B,H,S] fp32 or null
-  long long o_sb, o_sh, o_ss;
+  long long o_sb, o_sg, o_sh, o_ss;  // batch, head group, head within group, position
   int B, H, S, d;
-  int hs_swap;
+  int hg;                       // heads per group (divides H)
   bool bf16;
   float scale;                  // softmax scale (already resolved)
   unsigned* status;             // device status word

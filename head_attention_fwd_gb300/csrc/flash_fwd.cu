@@ -96,8 +96,9 @@ static_assert(Cfg<64>::COL_P + 128 <= 512, "tensor memory budget");
 struct Params {
   void* o;
   float* lse;
-  long long o_sb, o_sh, o_ss;
-  int H, S, n_qblk, hs_swap;
+  long long o_sb, o_sg, o_sh, o_ss;  // O: batch, head group, head within group, position
+  int H, S, n_qblk;
+  int hg, G;                           // heads per group, groups per batch (H = G * hg)
   float c;  // scale · log2(e)
   unsigned* status;
   long long limit;
@@ -127,6 +128,7 @@ __global__ void __launch_bounds__(352, 1)
   const int qblk = static_cast<int>(blockIdx.x) % p.n_qblk;
   const int bh = static_cast<int>(blockIdx.x) / p.n_qblk;
   const int b = bh / p.H, hh = bh % p.H;
+  const int hsub = hh % p.hg, bsup = b * p.G + hh / p.hg;  // tensor-map coordinates of this head
   const int q0 = qblk * (C::NQ * C::BM);
   const int n_kv = (p.S + C::BN - 1) / C::BN;
 
@@ -161,12 +163,10 @@ __global__ void __launch_bounds__(352, 1)
   const WaitCtx wc{abort_flag, p.status, p.limit};
   const bool skip = *abort_flag != 0;
 
-  // Coordinates (feature, row) -> tensor-map coordinates.
+  // (feature, position) -> tensor-map coordinates; the maps are
+  // (d, head within group, S, group and batch) for every layout.
   auto tma4 = [&](uint32_t dst, const CUtensorMap* m, uint32_t mbar, int e, int s) {
-    if (p.hs_swap)
-      tma_load_4d(dst, m, mbar, e, hh, s, b);
-    else
-      tma_load_4d(dst, m, mbar, e, s, hh, b);
+    tma_load_4d(dst, m, mbar, e, hsub, s, bsup);
   };
 
   if (skip) {
@@ -518,7 +518,7 @@ __global__ void __launch_bounds__(352, 1)
       const int row = q0 + t * C::BM + static_cast<int>(wq * 32 + lane);
       const bool in = row < p.S;
       using Elem = uint16_t;
-      Elem* out = static_cast<Elem*>(p.o) + b * p.o_sb + hh * p.o_sh +
+      Elem* out = static_cast<Elem*>(p.o) + b * p.o_sb + (hh / p.hg) * p.o_sg + hsub * p.o_sh +
                   static_cast<long long>(in ? row : 0) * p.o_ss;
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
@@ -558,12 +558,14 @@ cudaError_t launch_impl(const FlashLaunch& a, cudaStream_t st) {
   p.o = a.o;
   p.lse = a.lse;
   p.o_sb = a.o_sb;
+  p.o_sg = a.o_sg;
   p.o_sh = a.o_sh;
   p.o_ss = a.o_ss;
   p.H = a.H;
   p.S = a.S;
   p.n_qblk = (a.S + C::NQ * C::BM - 1) / (C::NQ * C::BM);
-  p.hs_swap = a.hs_swap;
+  p.hg = a.hg;
+  p.G = a.H / a.hg;
   p.c = a.scale * kLog2e;
   p.status = a.status;
   p.limit = a.limit;

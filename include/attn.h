@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-typedef enum { ATTN_LAYOUT_BHSD = 0, ATTN_LAYOUT_BSHD = 1 } attn_layout;
+typedef enum { ATTN_LAYOUT_BHSD = 0, ATTN_LAYOUT_BSHD = 1, ATTN_LAYOUT_GROUPED = 2 } attn_layout;
 typedef enum { ATTN_F32 = 0, ATTN_F16 = 1, ATTN_BF16 = 2 } attn_dtype;
 
 enum {
@@ -87,6 +87,19 @@ typedef enum { ATTN_KERNEL_NAIVE = 0, ATTN_KERNEL_ONLINE = 1 } attn_kernel;
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h, int S,
              int d, float scale, int layout, int dtype, void* stream);
+
+/*
+ * attn_fwd_grouped -- attn_fwd on the third layout of "WebGPU 算子优化：QKV
+ * 内存合并与 FlashAttention 分块计算", §QKV 矩阵的内存合并模式选择 ("split":
+ * heads in groups, each group stored contiguously).  q, k, v, o are
+ * [B, h/heads_per_group, S, heads_per_group, d]: per group, positions in
+ * order and the group's heads interleaved within a position.
+ * heads_per_group = 1 is the contiguous layout, = h the head-interleaved one.
+ * 16-bit dtypes only (ATTN_E_DTYPE for ATTN_F32); heads_per_group must divide
+ * h (ATTN_E_SHAPE).  Other arguments, lse and errors as attn_fwd.
+ */
+int attn_fwd_grouped(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h,
+                     int S, int d, int heads_per_group, float scale, int dtype, void* stream);
 
 /*
  * attn_fwd_naive -- the unfused "standard" attention the pages compare

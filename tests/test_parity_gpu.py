@@ -152,3 +152,32 @@ def test_back_to_back_calls_on_one_stream(dev):
     device_status_ok()
     for o in outs:
         assert torch.equal(o, o1)
+
+
+GROUPED = [(1, 4, 300, 64, 2), (2, 8, 257, 64, 4), (1, 6, 129, 128, 3), (1, 4, 200, 64, 1),
+           (1, 4, 200, 128, 4)]
+
+
+@pytest.mark.parametrize("shape", GROUPED, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
+def test_grouped_layout_matches_oracle(dev, shape, dtype):
+    """The head-group ("split") layout [B, h/hg, S, hg, d], hg = 1 and hg = h included."""
+    B, h, S, d, hg = shape
+    g = torch.Generator().manual_seed(h * S + hg)
+    q, k, v = (torch.randn((B, h // hg, S, hg, d), generator=g).to(dtype) for _ in range(3))
+    o, lse = attn.attn_fwd_grouped(q.to(dev), k.to(dev), v.to(dev), want_lse=True)
+    device_status_ok()
+    o_ref, lse_ref = oracle.attention_grouped(q, k, v, hg, scale=1 / math.sqrt(d))
+    check_o(o, o_ref, dtype, f"grouped {shape}")
+    check_lse(lse, lse_ref, f"grouped {shape}")
+
+
+def test_grouped_layout_rejects_bad_groups(dev):
+    import ctypes
+    L = attn.lib()
+    vp = ctypes.c_void_p
+    q = torch.zeros((1, 2, 64, 3, 64), dtype=torch.float32, device=dev)  # large enough for either dtype
+    o = torch.empty_like(q)
+    p, po = vp(q.data_ptr()), vp(o.data_ptr())
+    assert L.attn_fwd_grouped(p, p, p, po, None, 1, 6, 64, 64, 4, 0.0, 1, vp(0)) == -2  # 4 does not divide 6
+    assert L.attn_fwd_grouped(p, p, p, po, None, 1, 6, 64, 64, 3, 0.0, 0, vp(0)) == -5  # fp32: not supported

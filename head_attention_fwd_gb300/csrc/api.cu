@@ -206,36 +206,35 @@ void o_strides(int layout, long long H, long long S, long long d, long long rs, 
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Element strides of a [B,H,S,d] problem seen as heads in groups of hg
-// (see make_flash_map): layout 0 -> hg = 1, layout 1 -> hg = H with row
-// stride rs, layout 2 (head groups) -> the given hg.
-struct GroupedStrides {
-  long long hg, sb, sg, sh, ss;
-};
-GroupedStrides grouped_strides(int layout, long long H, long long S, long long d, long long rs,
-                               long long hg) {
-  if (layout == ATTN_LAYOUT_BHSD) return {1, H * S * d, S * d, d, d};
-  if (layout == ATTN_LAYOUT_BSHD) return {H, S * rs, S * rs, d, rs};
-  return {hg, H * S * d, S * hg * d, d, hg * d};
-}
-
 // Flash launch on tensors of a [B,H,S,d] problem; inputs and output may have
-// different row strides (rs_in, rs_out: layout 1 only).
+// different row strides (rs_in, rs_out: layout 1 only).  Layout
+// ATTN_LAYOUT_GROUPED takes hg heads per group ([B,H/hg,S,hg,d]).
 int run_flash(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h, int S,
               int d, float scale, int layout, long long hg, int dtype, long long rs_in,
               long long rs_out, unsigned* status, cudaStream_t st) {
   attn::FlashLaunch a;
-  const GroupedStrides gi = grouped_strides(layout, h, S, d, rs_in, hg);
-  int rc = make_flash_map(&a.tq, q, dtype, B, h, S, d, gi.hg, gi.sh, gi.ss, gi.sg);
-  if (!rc) rc = make_flash_map(&a.tk, k, dtype, B, h, S, d, gi.hg, gi.sh, gi.ss, gi.sg);
-  if (!rc) rc = make_flash_map(&a.tv, v, dtype, B, h, S, d, gi.hg, gi.sh, gi.ss, gi.sg);
+  int rc = ATTN_OK;
+  a.grouped = layout == ATTN_LAYOUT_GROUPED;
+  a.hs_swap = 0;
+  a.hg = 1;
+  if (a.grouped) {
+    const long long sh = d, ss = hg * d, sg = S * hg * d;
+    rc = make_flash_map(&a.tq, q, dtype, B, h, S, d, hg, sh, ss, sg);
+    if (!rc) rc = make_flash_map(&a.tk, k, dtype, B, h, S, d, hg, sh, ss, sg);
+    if (!rc) rc = make_flash_map(&a.tv, v, dtype, B, h, S, d, hg, sh, ss, sg);
+    a.o_sb = static_cast<long long>(h) * S * d, a.o_sg = sg, a.o_sh = sh, a.o_ss = ss;
+    a.hg = static_cast<int>(hg);
+  } else {
+    rc = make_map(&a.tq, q, dtype, layout, B, h, S, d, rs_in, 128, &a.hs_swap);
+    if (!rc) rc = make_map(&a.tk, k, dtype, layout, B, h, S, d, rs_in, 128, &a.hs_swap);
+    if (!rc) rc = make_map(&a.tv, v, dtype, layout, B, h, S, d, rs_in, 128, &a.hs_swap);
+    o_strides(layout, h, S, d, rs_out, &a.o_sb, &a.o_sh, &a.o_ss);
+    a.o_sg = 0;
+  }
   if (rc) return rc;
-  const GroupedStrides go = grouped_strides(layout, h, S, d, rs_out, hg);
   a.o = o;
   a.lse = lse;
-  a.o_sb = go.sb, a.o_sg = go.sg, a.o_sh = go.sh, a.o_ss = go.ss;
   a.B = B, a.H = h, a.S = S, a.d = d;
-  a.hg = static_cast<int>(gi.hg);
   a.bf16 = dtype == ATTN_BF16;
   a.scale = scale;
   a.status = status;
@@ -323,8 +322,9 @@ int attn_fwd_naive(const void* q, const void* k, const void* v, void* o, float* 
   // 1. S = scale · Q·K^T  (fp32, [B,H,S,sp])
   attn::GemmLaunch g1;
   int swap = 0;
+  const int bn1 = S >= 256 ? 256 : 128;  // key block of the S tile (the K map's box height)
   rc = make_map(&g1.ta, q, dtype, layout, B, h, S, d, rs, 128, &swap);
-  if (!rc) rc = make_map(&g1.tb, k, dtype, layout, B, h, S, d, rs, 128, &swap);
+  if (!rc) rc = make_map(&g1.tb, k, dtype, layout, B, h, S, d, rs, bn1, &swap);
   if (rc) return rc;
   g1.c = s_mat;
   g1.c_type = 0;
@@ -332,7 +332,7 @@ int attn_fwd_naive(const void* q, const void* k, const void* v, void* o, float* 
   g1.c_s1 = S * sp;
   g1.c_s2 = static_cast<long long>(h) * S * sp;
   g1.M = S, g1.N = S, g1.K = d, g1.Z1 = h, g1.Z2 = B;
-  g1.bn = 128;
+  g1.bn = bn1;
   g1.b_kmajor = true;
   g1.a_swap = g1.b_swap = swap;
   g1.bf16 = dtype == ATTN_BF16;
@@ -412,7 +412,7 @@ int qkv_proj_attn(const void* x, const void* w_qkv, void* o, int B, int S, int D
   g.ldc = 3LL * D;
   g.c_s1 = g.c_s2 = 0;
   g.M = static_cast<int>(rows), g.N = 3 * D, g.K = D, g.Z1 = 1, g.Z2 = 1;
-  g.bn = 128;
+  g.bn = (3 * D) % 256 == 0 ? 256 : 128;
   g.b_kmajor = false;
   g.a_swap = g.b_swap = 0;
   g.bf16 = dtype == ATTN_BF16;

@@ -7,19 +7,21 @@
 
 namespace attn {
 
-// Tensor maps of the attention kernel: every layout is seen as heads in
-// groups of hg, dims (d, hg, S, (H/hg)·B) -- feature, head within the group,
-// position, then group and batch merged (the batch stride is always H/hg
-// group strides).  Contiguous [B,H,S,d] is hg = 1, head-interleaved
-// [B,S,H,d] is hg = H, and the head-group layout [B,H/hg,S,hg,d] is general.
+// Tensor maps of the attention kernel.  Layouts 0/1: dims (d, S, H, B)
+// (contiguous [B,H,S,d], hs_swap = 0) or (d, H, S, B) (head-interleaved
+// [B,S,H,d], hs_swap = 1), so that byte strides grow with the dimension.
+// Grouped layout [B,H/hg,S,hg,d]: dims (d, hg, S, (H/hg)·B) -- feature, head
+// within the group, position, then group and batch merged.
 
 struct FlashLaunch {
-  CUtensorMap tq, tk, tv;       // 4-d maps, box = 64 features x 1 x 128 positions x 1
+  CUtensorMap tq, tk, tv;       // 4-d maps, box = 64 features x 128 positions
   void* o;                      // output, element strides below (feature stride 1)
   float* lse;                   // [B,H,S] fp32 or null
-  long long o_sb, o_sg, o_sh, o_ss;  // batch, head group, head within group, position
+  long long o_sb, o_sg, o_sh, o_ss;  // batch, head group (grouped only), head, position
   int B, H, S, d;
-  int hg;                       // heads per group (divides H)
+  bool grouped;
+  int hs_swap;                  // layouts 0/1
+  int hg;                       // grouped: heads per group (divides H)
   bool bf16;
   float scale;                  // softmax scale (already resolved)
   unsigned* status;             // device status word

@@ -96,9 +96,10 @@ static_assert(Cfg<64>::COL_P + 128 <= 512, "tensor memory budget");
 struct Params {
   void* o;
   float* lse;
-  long long o_sb, o_sg, o_sh, o_ss;  // O: batch, head group, head within group, position
+  long long o_sb, o_sg, o_sh, o_ss;  // O: batch, head group (grouped only), head, position
   int H, S, n_qblk;
-  int hg, G;                           // heads per group, groups per batch (H = G * hg)
+  int hs_swap;                         // layouts 0/1: tensor-map dims (d, H, S, B) instead of (d, S, H, B)
+  int hg, G;                           // grouped layout: heads per group, groups per batch
   float c;  // scale · log2(e)
   unsigned* status;
   long long limit;
@@ -111,7 +112,7 @@ __device__ __forceinline__ uint32_t code_of(uint32_t role, int j) {
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 __device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool GROUPED>
 __global__ void __launch_bounds__(352, 1)
     flash_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      const __grid_constant__ CUtensorMap tv, const Params p) {
@@ -128,7 +129,6 @@ __global__ void __launch_bounds__(352, 1)
   const int qblk = static_cast<int>(blockIdx.x) % p.n_qblk;
   const int bh = static_cast<int>(blockIdx.x) / p.n_qblk;
   const int b = bh / p.H, hh = bh % p.H;
-  const int hsub = hh % p.hg, bsup = b * p.G + hh / p.hg;  // tensor-map coordinates of this head
   const int q0 = qblk * (C::NQ * C::BM);
   const int n_kv = (p.S + C::BN - 1) / C::BN;
 
@@ -163,16 +163,22 @@ __global__ void __launch_bounds__(352, 1)
   const WaitCtx wc{abort_flag, p.status, p.limit};
   const bool skip = *abort_flag != 0;
 
-  // (feature, position) -> tensor-map coordinates; the maps are
-  // (d, head within group, S, group and batch) for every layout.
-  auto tma4 = [&](uint32_t dst, const CUtensorMap* m, uint32_t mbar, int e, int s) {
-    tma_load_4d(dst, m, mbar, e, hsub, s, bsup);
-  };
 
   if (skip) {
     // nothing
   } else if (warp == 8) {
     // ------------------------------------------------------ TMA producer ----
+    // (feature, position) -> tensor-map coordinates.  Layouts 0/1: maps
+    // (d, S, H, B) or (d, H, S, B); grouped: (d, head within group, S,
+    // group and batch).
+    auto tma4 = [&](uint32_t dst, const CUtensorMap* m, uint32_t mbar, int e, int s) {
+      if constexpr (GROUPED)
+        tma_load_4d(dst, m, mbar, e, hh % p.hg, s, b * p.G + hh / p.hg);
+      else if (p.hs_swap)
+        tma_load_4d(dst, m, mbar, e, hh, s, b);
+      else
+        tma_load_4d(dst, m, mbar, e, s, hh, b);
+    };
     if (lane == 0) {
       prefetch_tmap(&tq);
       prefetch_tmap(&tk);
@@ -518,7 +524,9 @@ __global__ void __launch_bounds__(352, 1)
       const int row = q0 + t * C::BM + static_cast<int>(wq * 32 + lane);
       const bool in = row < p.S;
       using Elem = uint16_t;
-      Elem* out = static_cast<Elem*>(p.o) + b * p.o_sb + (hh / p.hg) * p.o_sg + hsub * p.o_sh +
+      const long long head_off = GROUPED ? (hh / p.hg) * p.o_sg + (hh % p.hg) * p.o_sh
+                                         : static_cast<long long>(hh) * p.o_sh;
+      Elem* out = static_cast<Elem*>(p.o) + b * p.o_sb + head_off +
                   static_cast<long long>(in ? row : 0) * p.o_ss;
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
@@ -548,10 +556,10 @@ __global__ void __launch_bounds__(352, 1)
   }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool GROUPED>
 cudaError_t launch_impl(const FlashLaunch& a, cudaStream_t st) {
   using C = Cfg<D>;
-  auto kern = flash_fwd_kernel<D, BF16>;
+  auto kern = flash_fwd_kernel<D, BF16, GROUPED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   Params p;
@@ -564,6 +572,7 @@ cudaError_t launch_impl(const FlashLaunch& a, cudaStream_t st) {
   p.H = a.H;
   p.S = a.S;
   p.n_qblk = (a.S + C::NQ * C::BM - 1) / (C::NQ * C::BM);
+  p.hs_swap = a.hs_swap;
   p.hg = a.hg;
   p.G = a.H / a.hg;
   p.c = a.scale * kLog2e;
@@ -576,10 +585,15 @@ cudaError_t launch_impl(const FlashLaunch& a, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_flash_fwd(const FlashLaunch& a, cudaStream_t st) {
-  if (a.d == 64) return a.bf16 ? launch_impl<64, true>(a, st) : launch_impl<64, false>(a, st);
-  if (a.d == 128) return a.bf16 ? launch_impl<128, true>(a, st) : launch_impl<128, false>(a, st);
+template <bool G>
+cudaError_t launch_g(const FlashLaunch& a, cudaStream_t st) {
+  if (a.d == 64) return a.bf16 ? launch_impl<64, true, G>(a, st) : launch_impl<64, false, G>(a, st);
+  if (a.d == 128) return a.bf16 ? launch_impl<128, true, G>(a, st) : launch_impl<128, false, G>(a, st);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_flash_fwd(const FlashLaunch& a, cudaStream_t st) {
+  return a.grouped ? launch_g<true>(a, st) : launch_g<false>(a, st);
 }
 
 }  // namespace attn

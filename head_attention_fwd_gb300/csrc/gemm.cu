@@ -5,13 +5,17 @@
 // two products of the unfused comparison path (S = Q·K^T and O = P·V, same
 // chapter §2.2 and §2.4).
 //
-// One 128 x BN output tile per CTA, 6 warps, two CTAs per SM:
+// Persistent: one CTA per SM walks the 128 x BN output tiles (tile index
+// blockIdx.x, + gridDim.x, ...), 10 warps:
 //   warp 0     TMA producer: A (128 x 64, K-major) and B tiles through a
-//              3-stage ring of 128-byte-swizzled shared-memory buffers;
-//   warp 1     tcgen05 issuer, fp32 accumulator of 128 lanes x BN columns
-//              in tensor memory;
-//   warps 2-5  epilogue: tensor memory -> registers -> alpha, convert ->
-//              global (one thread per output row).
+//              STAGES-deep ring of 128-byte-swizzled shared-memory buffers,
+//              continuing across tiles;
+//   warp 1     tcgen05 issuer into one of two fp32 accumulators in tensor
+//              memory (128 lanes x BN columns each), alternating per tile;
+//   warps 2-9  epilogue: accumulator -> registers -> alpha, convert ->
+//              global (one thread per output row, two warps per tensor-memory
+//              lane quarter splitting the columns), while the issuer already
+//              fills the other accumulator with the next tile.
 // B is either K-major ([N, K], e.g. K of S = Q·K^T) or MN-major ([K, N],
 // e.g. W_qkv or V) -- the tensor cores read both directly.
 
@@ -23,28 +27,34 @@ namespace {
 
 template <int BN, bool BK>
 struct GCfg {
-  static constexpr int BM = 128, BKE = 64, STAGES = 3;
+  static constexpr int BM = 128, BKE = 64;
+  static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 5 : 6);
   static constexpr uint32_t A_BYTES = BM * 128;        // 128 rows x 64 elements x 2 B
   static constexpr uint32_t B_BYTES = BN * 128;        // BN x 64 x 2 B (either major)
   static constexpr uint32_t B_CHUNK = 64 * 128;        // MN-major: 64 k-rows x 64 n
   static constexpr uint32_t STAGE = A_BYTES + B_BYTES;
   static constexpr uint32_t OFF_BAR = STAGES * STAGE;
-  static constexpr int NBAR = 2 * STAGES + 2;          // full[], empty[], acc_full, drain
+  // full[], empty[], acc_full[2], acc_empty[2], drain
+  static constexpr int NBAR = 2 * STAGES + 5;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t SMEM = OFF_MISC + 16 + 1024;
-  static constexpr uint32_t TMEM_COLS = BN < 32 ? 32 : BN;
+  static constexpr uint32_t TMEM_COLS = 2 * BN;        // two accumulators
   __host__ __device__ static constexpr int bar_full(int s) { return s; }
   __host__ __device__ static constexpr int bar_empty(int s) { return STAGES + s; }
-  __host__ __device__ static constexpr int bar_acc() { return 2 * STAGES; }
-  __host__ __device__ static constexpr int bar_drain() { return 2 * STAGES + 1; }
+  __host__ __device__ static constexpr int bar_accfull(int a) { return 2 * STAGES + a; }
+  __host__ __device__ static constexpr int bar_accempty(int a) { return 2 * STAGES + 2 + a; }
+  __host__ __device__ static constexpr int bar_drain() { return 2 * STAGES + 4; }
 };
+static_assert(GCfg<256, false>::SMEM <= 227 * 1024, "shared memory budget");
+static_assert(GCfg<128, false>::SMEM <= 227 * 1024, "shared memory budget");
+static_assert(GCfg<64, false>::SMEM <= 227 * 1024, "shared memory budget");
 
 struct Params {
   void* c;
   int c_type;
   long long ldc, c_s1, c_s2;
   int M, N, K, Z1;
-  int n_mblk, n_nblk;
+  int n_mblk, n_nblk, n_tiles;
   int a_swap, b_swap;  // tensor-map dims (inner, Z1, rows, Z2) instead of (inner, rows, Z1, Z2)
   float alpha;
   unsigned* status;
@@ -56,7 +66,7 @@ __device__ __forceinline__ uint32_t gcode(uint32_t role, int j) {
 }
 
 template <int BN, bool BKMAJOR, bool BF16>
-__global__ void __launch_bounds__(192, 2)
+__global__ void __launch_bounds__(320, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
                 const Params p) {
   using C = GCfg<BN, BKMAJOR>;
@@ -69,19 +79,23 @@ __global__ void __launch_bounds__(192, 2)
   auto bar = [&](int i) -> uint32_t { return sb + C::OFF_BAR + 8u * static_cast<uint32_t>(i); };
 
   const uint32_t warp = warp_id(), lane = lane_id();
-  const int nb = static_cast<int>(blockIdx.x) % p.n_nblk;
-  const int mb = (static_cast<int>(blockIdx.x) / p.n_nblk) % p.n_mblk;
-  const int z = static_cast<int>(blockIdx.x) / (p.n_nblk * p.n_mblk);
-  const int z1 = z % p.Z1, z2 = z / p.Z1;
-  const int m0 = mb * C::BM, n0 = nb * BN;
   const int nk = (p.K + C::BKE - 1) / C::BKE;
+  // tile index -> (z, m block, n block), n fastest
+  auto tile_coords = [&](int tile, int& z, int& mb, int& nb) {
+    nb = tile % p.n_nblk;
+    mb = (tile / p.n_nblk) % p.n_mblk;
+    z = tile / (p.n_nblk * p.n_mblk);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar(C::bar_full(s)), 1);
       mbar_init(bar(C::bar_empty(s)), 1);
     }
-    mbar_init(bar(C::bar_acc()), 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar(C::bar_accfull(a)), 1);
+      mbar_init(bar(C::bar_accempty(a)), 8);  // one arrival per epilogue warp
+    }
     mbar_init(bar(C::bar_drain()), 1);
     *abort_flag = (*reinterpret_cast<volatile unsigned*>(p.status) != 0u) ? 1 : 0;
     fence_mbar_init();
@@ -97,82 +111,105 @@ __global__ void __launch_bounds__(192, 2)
   const WaitCtx wc{abort_flag, p.status, p.limit};
   const bool skip = *abort_flag != 0;
 
-  auto load = [&](uint32_t dst, const CUtensorMap* m, uint32_t mbar, int inner, int row, int swap) {
-    if (swap)
-      tma_load_4d(dst, m, mbar, inner, z1, row, z2);
-    else
-      tma_load_4d(dst, m, mbar, inner, row, z1, z2);
-  };
-
   if (skip) {
   } else if (warp == 0) {
+    // ------------------------------------------------------ TMA producer ----
     if (lane == 0) {
       prefetch_tmap(&ta);
       prefetch_tmap(&tb);
     }
-    int issued = 0;
+    int g = 0;  // k-steps issued so far (all tiles)
     bool ok = true;
-    for (int kt = 0; kt < nk; ++kt) {
-      const int s = kt % C::STAGES, u = kt / C::STAGES;
-      if (u > 0) ok = mbar_wait_warp(bar(C::bar_empty(s)), (u - 1) & 1, wc, gcode(ROLE_LOAD, kt));
-      if (!ok) break;
-      if (lane == 0) {
-        const uint32_t st = sb + s * C::STAGE;
-        mbar_expect_tx(bar(C::bar_full(s)), C::STAGE);
-        load(st, &ta, bar(C::bar_full(s)), kt * C::BKE, m0, p.a_swap);
-        if constexpr (BKMAJOR) {
-          load(st + C::A_BYTES, &tb, bar(C::bar_full(s)), kt * C::BKE, n0, p.b_swap);
-        } else {
+    for (int tile = blockIdx.x; tile < p.n_tiles && ok; tile += gridDim.x) {
+      int z, mb, nb;
+      tile_coords(tile, z, mb, nb);
+      const int z1 = z % p.Z1, z2 = z / p.Z1;
+      auto load = [&](uint32_t dst, const CUtensorMap* m, uint32_t mbar, int inner, int row, int swap) {
+        if (swap)
+          tma_load_4d(dst, m, mbar, inner, z1, row, z2);
+        else
+          tma_load_4d(dst, m, mbar, inner, row, z1, z2);
+      };
+      for (int kt = 0; kt < nk; ++kt, ++g) {
+        const int s = g % C::STAGES, u = g / C::STAGES;
+        if (u > 0 && !(ok = mbar_wait_warp(bar(C::bar_empty(s)), (u - 1) & 1, wc, gcode(ROLE_LOAD, g))))
+          break;
+        if (lane == 0) {
+          const uint32_t st = sb + s * C::STAGE;
+          mbar_expect_tx(bar(C::bar_full(s)), C::STAGE);
+          load(st, &ta, bar(C::bar_full(s)), kt * C::BKE, mb * C::BM, p.a_swap);
+          if constexpr (BKMAJOR) {
+            load(st + C::A_BYTES, &tb, bar(C::bar_full(s)), kt * C::BKE, nb * BN, p.b_swap);
+          } else {
 #pragma unroll
-          for (int c = 0; c < BN / 64; ++c)
-            load(st + C::A_BYTES + c * C::B_CHUNK, &tb, bar(C::bar_full(s)), n0 + c * 64,
-                 kt * C::BKE, p.b_swap);
+            for (int c = 0; c < BN / 64; ++c)
+              load(st + C::A_BYTES + c * C::B_CHUNK, &tb, bar(C::bar_full(s)), nb * BN + c * 64,
+                   kt * C::BKE, p.b_swap);
+          }
         }
       }
-      issued = kt + 1;
     }
-    if (!ok) {
-      const WaitCtx drain{abort_flag, p.status, p.limit};
-      for (int kt = issued - C::STAGES < 0 ? 0 : issued - C::STAGES; kt < issued; ++kt)
-        mbar_wait_slow(bar(C::bar_full(kt % C::STAGES)), (kt / C::STAGES) & 1, drain, 0, false);
+    if (!ok) {  // let the copies in flight land before the CTA can exit
+      for (int q = g - C::STAGES < 0 ? 0 : g - C::STAGES; q < g; ++q)
+        mbar_wait_slow(bar(C::bar_full(q % C::STAGES)), (q / C::STAGES) & 1, wc, 0, false);
     }
   } else if (warp == 1) {
+    // ------------------------------------------------- tcgen05 issuer ----
     // The whole warp runs the issue loop; elect.sync inside the helpers picks
     // the lane that issues, so the descriptors stay warp-uniform.
     constexpr uint32_t idesc = idesc_f16(128, BN, BF16, false, !BKMAJOR);
     const uint64_t da = sdesc_sw128(sb, 16, 1024);
     const uint64_t db = BKMAJOR ? sdesc_sw128(sb + C::A_BYTES, 16, 1024)
                                 : sdesc_sw128(sb + C::A_BYTES, C::B_CHUNK, 1024);
+    int g = 0, i = 0;  // k-steps consumed, tiles done by this CTA
     bool ok = true;
-    for (int kt = 0; kt < nk; ++kt) {
-      const int s = kt % C::STAGES, u = kt / C::STAGES;
-      ok = mbar_wait_warp(bar(C::bar_full(s)), u & 1, wc, gcode(ROLE_MMA, kt));
-      if (!ok) break;
+    for (int tile = blockIdx.x; tile < p.n_tiles && ok; tile += gridDim.x, ++i) {
+      const int a = i & 1;
+      if (i >= 2 && !(ok = mbar_wait_warp(bar(C::bar_accempty(a)), ((i >> 1) - 1) & 1, wc,
+                                         gcode(ROLE_MMA, i))))
+        break;
       tc_fence_after();
-      const uint32_t st16 = (s * C::STAGE) >> 4;  // stage offset in descriptor address units
+      const uint32_t acc = tmem + a * BN;
+      for (int kt = 0; kt < nk; ++kt, ++g) {
+        const int s = g % C::STAGES, u = g / C::STAGES;
+        if (!(ok = mbar_wait_warp(bar(C::bar_full(s)), u & 1, wc, gcode(ROLE_MMA, g)))) break;
+        tc_fence_after();
+        const uint32_t st16 = (s * C::STAGE) >> 4;  // stage offset in descriptor address units
 #pragma unroll
-      for (int kk = 0; kk < C::BKE / 16; ++kk) {
-        const uint32_t ka = (kk * 32) >> 4, kb = (BKMAJOR ? kk * 32 : kk * 2048) >> 4;
-        mma_ss_elect(tmem, da + st16 + ka, db + st16 + kb, idesc, (kt > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < C::BKE / 16; ++kk) {
+          const uint32_t ka = (kk * 32) >> 4, kb = (BKMAJOR ? kk * 32 : kk * 2048) >> 4;
+          mma_ss_elect(acc, da + st16 + ka, db + st16 + kb, idesc, (kt > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit_elect(bar(C::bar_empty(s)));
       }
-      mma_commit_elect(bar(C::bar_empty(s)));
+      if (ok) mma_commit_elect(bar(C::bar_accfull(a)));
     }
-    mma_commit_elect(bar(ok ? C::bar_acc() : C::bar_drain()));
-    if (!ok) mbar_wait_slow(bar(C::bar_drain()), 0, wc, 0, false);
+    if (!ok) {
+      mma_commit_elect(bar(C::bar_drain()));
+      mbar_wait_slow(bar(C::bar_drain()), 0, wc, 0, false);
+    }
   } else {
     // -------------------------------------------------------- epilogue ----
-    const uint32_t wq = warp & 3u;
-    if (mbar_wait_warp(bar(C::bar_acc()), 0, wc, gcode(ROLE_EPILOGUE, 0))) {
+    const uint32_t wq = warp & 3u;               // tensor-memory lane quarter
+    const int half = (static_cast<int>(warp) - 2) >> 2;  // which half of the column chunks
+    int i = 0;
+    for (int tile = blockIdx.x; tile < p.n_tiles; tile += gridDim.x, ++i) {
+      const int a = i & 1;
+      if (!mbar_wait_warp(bar(C::bar_accfull(a)), (i >> 1) & 1, wc, gcode(ROLE_EPILOGUE, i))) break;
       tc_fence_after();
-      const int row = m0 + static_cast<int>(wq * 32 + lane);
+      int z, mb, nb;
+      tile_coords(tile, z, mb, nb);
+      const int z1 = z % p.Z1, z2 = z / p.Z1;
+      const int row = mb * C::BM + static_cast<int>(wq * 32 + lane);
       const bool in = row < p.M;
       const long long off = z2 * p.c_s2 + z1 * p.c_s1 + static_cast<long long>(in ? row : 0) * p.ldc;
+      const uint32_t acc = tmem + ((wq * 32u) << 16) + a * BN;
 #pragma unroll 1
-      for (int cc = 0; cc < BN / 32; ++cc) {
+      for (int cc = half * (BN / 64); cc < (half + 1) * (BN / 64); ++cc) {
         uint32_t r[32];
-        tmem_ld32(tmem + ((wq * 32u) << 16) + cc * 32, r);
+        tmem_ld32(acc + cc * 32, r);
         tmem_ld_wait(r);
-        const int col0 = n0 + cc * 32;
+        const int col0 = nb * BN + cc * 32;
         if (!in || col0 >= p.N) continue;
         const int nvalid = min(32, p.N - col0);
         if (p.c_type == 0) {
@@ -180,22 +217,21 @@ __global__ void __launch_bounds__(192, 2)
           const bool vec = nvalid == 32 && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0;
           if (vec) {
 #pragma unroll
-            for (int i = 0; i < 32; i += 4)
-              *reinterpret_cast<float4*>(dst + i) =
-                  make_float4(__uint_as_float(r[i]) * p.alpha, __uint_as_float(r[i + 1]) * p.alpha,
-                              __uint_as_float(r[i + 2]) * p.alpha, __uint_as_float(r[i + 3]) * p.alpha);
+            for (int k = 0; k < 32; k += 4)
+              *reinterpret_cast<float4*>(dst + k) =
+                  make_float4(__uint_as_float(r[k]) * p.alpha, __uint_as_float(r[k + 1]) * p.alpha,
+                              __uint_as_float(r[k + 2]) * p.alpha, __uint_as_float(r[k + 3]) * p.alpha);
           } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (i < nvalid) dst[i] = __uint_as_float(r[i]) * p.alpha;
+            for (int k = 0; k < 32; ++k)
+              if (k < nvalid) dst[k] = __uint_as_float(r[k]) * p.alpha;
           }
         } else {
           uint16_t* dst = static_cast<uint16_t*>(p.c) + off + col0;
           uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = pack2<BF16>(__uint_as_float(r[2 * i]) * p.alpha,
-                                __uint_as_float(r[2 * i + 1]) * p.alpha);
+          for (int k = 0; k < 16; ++k)
+            pk[k] = pack2<BF16>(__uint_as_float(r[2 * k]) * p.alpha, __uint_as_float(r[2 * k + 1]) * p.alpha);
           const bool vec = nvalid == 32 && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0;
           if (vec) {
 #pragma unroll
@@ -204,11 +240,15 @@ __global__ void __launch_bounds__(192, 2)
                   make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
           } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (i < nvalid) dst[i] = static_cast<uint16_t>(pk[i >> 1] >> ((i & 1) * 16));
+            for (int k = 0; k < 32; ++k)
+              if (k < nvalid) dst[k] = static_cast<uint16_t>(pk[k >> 1] >> ((k & 1) * 16));
           }
         }
       }
+      // this accumulator may be overwritten by the tile after next
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::bar_accempty(a)));
     }
   }
 
@@ -218,6 +258,19 @@ __global__ void __launch_bounds__(192, 2)
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
+}
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+      n = v;
+    else
+      n = 148;
+  }
+  return n;
 }
 
 template <int BN, bool BKMAJOR, bool BF16>
@@ -238,13 +291,16 @@ cudaError_t launch_impl(const GemmLaunch& a, cudaStream_t st) {
   p.Z1 = a.Z1;
   p.n_mblk = (a.M + C::BM - 1) / C::BM;
   p.n_nblk = (a.N + BN - 1) / BN;
+  const long long tiles = static_cast<long long>(p.n_mblk) * p.n_nblk * a.Z1 * a.Z2;
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+  p.n_tiles = static_cast<int>(tiles);
   p.a_swap = a.a_swap;
   p.b_swap = a.b_swap;
   p.alpha = a.alpha;
   p.status = a.status;
   p.limit = a.limit;
-  const long long grid = static_cast<long long>(p.n_mblk) * p.n_nblk * a.Z1 * a.Z2;
-  kern<<<static_cast<unsigned>(grid), 192, C::SMEM, st>>>(a.ta, a.tb, p);
+  const int grid = static_cast<int>(tiles < num_sms() ? tiles : num_sms());
+  kern<<<grid, 320, C::SMEM, st>>>(a.ta, a.tb, p);
   return cudaGetLastError();
 }
 
@@ -253,6 +309,8 @@ cudaError_t dispatch(const GemmLaunch& a, cudaStream_t st) {
   if (a.bn == 64) return a.b_kmajor ? launch_impl<64, true, BF16>(a, st) : launch_impl<64, false, BF16>(a, st);
   if (a.bn == 128)
     return a.b_kmajor ? launch_impl<128, true, BF16>(a, st) : launch_impl<128, false, BF16>(a, st);
+  if (a.bn == 256)
+    return a.b_kmajor ? launch_impl<256, true, BF16>(a, st) : launch_impl<256, false, BF16>(a, st);
   return cudaErrorInvalidValue;
 }
 

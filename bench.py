@@ -245,10 +245,11 @@ def run_ours(args):
                    for _ in range(3))
         sets.append((q, k, v, torch.empty_like(q)))
     set_bytes = sum(t.numel() * t.element_size() for t in sets[0])
+    ws = split_scratch(attn, w, dev)
 
     def step(i):
         q, k, v, o = sets[i % N_SETS]
-        attn.attn_fwd(q, k, v, o, layout=w.layout, stream=stream)
+        attn.attn_fwd(q, k, v, o, layout=w.layout, stream=stream, workspace=ws)
 
     for i in range(args.warmup):
         step(i)
@@ -291,7 +292,7 @@ def run_ours(args):
         "kernel_source_hash": khash,
     }
 
-    e2e = run_e2e(attn, w, sets, stream, flops_step, args.steps)
+    e2e = run_e2e(attn, w, sets, stream, flops_step, args.steps, ws)
 
     extra = {}
     if not args.no_extra and world == 1:
@@ -304,7 +305,10 @@ def run_ours(args):
         "config": {"workload": w.name, "B": w.B, "h": w.h, "S": w.S, "d": w.d, "layout": "BHSD",
                    "causal": False, "scale": w.scale, "global_batch": w.B * world,
                    "parallelism": f"independent problem per rank x{world} (no collective)",
-                   "l2": f"{N_SETS} rotating input sets, {N_SETS * set_bytes / 2**20:.0f} MiB > 129 MB L2"},
+                   "l2": f"{N_SETS} rotating input sets, {N_SETS * set_bytes / 2**20:.0f} MiB > 129 MB L2",
+                   "schedule": ("persistent; last waves cut along keys "
+                                f"({ws.numel() / 2**20:.1f} MiB scratch, attn_fwd_ws)") if ws is not None
+                   else "persistent; whole items (attn_fwd)"},
         "gpu_launches": args.steps,
         "roofline": roofline,
         "clocks": clocks,
@@ -321,7 +325,7 @@ def run_ours(args):
     barrier(world)
 
 
-def run_e2e(attn, w, sets, stream, flops_step, steps):
+def run_e2e(attn, w, sets, stream, flops_step, steps, ws):
     """The same metric through the public call with pinned HOST buffers: every
     step uploads its Q, K, V (H2D) and downloads its O (D2H) inside the timed
     region.  As a user of the library would, the steps are pipelined over two
@@ -348,7 +352,7 @@ def run_e2e(attn, w, sets, stream, flops_step, steps):
             ev_up[b].record(up)
         stream.wait_event(ev_up[b])
         stream.wait_event(ev_down[b])            # O of step i-nb has been downloaded
-        attn.attn_fwd(qd, kd, vd, od, layout=w.layout, stream=stream)
+        attn.attn_fwd(qd, kd, vd, od, layout=w.layout, stream=stream, workspace=ws)
         ev_comp[b].record(stream)
         with torch.cuda.stream(down):
             down.wait_event(ev_comp[b])
@@ -380,6 +384,14 @@ def run_e2e(attn, w, sets, stream, flops_step, steps):
             "ms_per_step": t / n * 1e3}
 
 
+def split_scratch(attn, w, dev):
+    """Scratch that lets attn_fwd cut the last wave of items along the key
+    axis (None when the item count already fills whole waves)."""
+    import torch
+    need = attn.attn_fwd_ws_bytes(w.B, w.h, w.S, w.d, w.torch_dtype)
+    return torch.empty(need, dtype=torch.uint8, device=dev) if need else None
+
+
 def run_extra(attn, w, sets, stream, dev):
     """Unfused comparison on the same workload and fused throughput on the
     other tensor-core workloads (each timed alone with CUDA events)."""
@@ -398,19 +410,27 @@ def run_extra(attn, w, sets, stream, dev):
     out["naive_two_pass_" + w.name] = {"tflops": w.attn_flops * n / t / 1e12, "ms": t / n * 1e3,
                                        "launches_per_call": 4}
     del ws
+    # the same workload through attn_fwd (whole items only, no scratch)
+    for _ in range(3):
+        attn.attn_fwd(q, k, v, o, layout=w.layout, stream=stream, split=False)
+    n = 200
+    t = time_launches(lambda i: attn.attn_fwd(*sets[i % N_SETS], layout=w.layout, stream=stream,
+                                              split=False), n, stream)
+    out[w.name + "_whole_items"] = {"tflops": w.attn_flops * n / t / 1e12, "ms": t / n * 1e3}
     for name in ("long_seq_bf16_peaky", "wide_head_bf16_bshd"):
         ww = WORKLOADS[name]
         g = torch.Generator(device=dev).manual_seed(ww.seed)
         qq, kk, vv = (torch.randn(ww.shape(), generator=g, device=dev).to(ww.torch_dtype) for _ in range(3))
         oo = torch.empty_like(qq)
         lse = torch.empty((ww.B, ww.h, ww.S), dtype=torch.float32, device=dev) if ww.want_lse else None
+        wsx = split_scratch(attn, ww, dev)
         for _ in range(3):
-            attn.attn_fwd(qq, kk, vv, oo, lse, layout=ww.layout, stream=stream)
+            attn.attn_fwd(qq, kk, vv, oo, lse, layout=ww.layout, stream=stream, workspace=wsx)
         n = 20
-        t = time_launches(lambda i: attn.attn_fwd(qq, kk, vv, oo, lse, layout=ww.layout, stream=stream),
-                          n, stream)
+        t = time_launches(lambda i: attn.attn_fwd(qq, kk, vv, oo, lse, layout=ww.layout, stream=stream,
+                                                  workspace=wsx), n, stream)
         out[name] = {"tflops": ww.attn_flops * n / t / 1e12, "ms": t / n * 1e3}
-        del qq, kk, vv, oo, lse
+        del qq, kk, vv, oo, lse, wsx
     wb = WORKLOADS["bert_base_qkv"]
     g = torch.Generator(device=dev).manual_seed(wb.seed)
     x = torch.randn((wb.B, wb.S, wb.D), generator=g, device=dev).to(wb.torch_dtype)

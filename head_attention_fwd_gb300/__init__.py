@@ -7,7 +7,8 @@ no fallback: if the library is not built, every call raises.
 
 Entry points (same names as the C ABI):
 
-* ``attn_fwd(q, k, v, ...)``        fused online-softmax attention
+* ``attn_fwd(q, k, v, ...)``        fused online-softmax attention (through
+  ``attn_fwd_ws`` with a small scratch unless ``split=False``)
 * ``attn_fwd_naive(q, k, v, ...)``  unfused two-pass-softmax comparison path
 * ``qkv_proj_attn(x, w_qkv, h, ...)`` fused QKV projection, then attention
 * ``qkv_proj_attn_noalloc(x, w_qkv, h, ...)`` the same without a workspace argument
@@ -55,6 +56,10 @@ def lib() -> ctypes.CDLL:
             vp, ci, cf, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
             L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, cf, ci, ci, vp]
             L.attn_fwd.restype = ci
+            L.attn_fwd_ws.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, cf, ci, ci, vp, sz, vp]
+            L.attn_fwd_ws.restype = ci
+            L.attn_fwd_ws_bytes.argtypes = [ci, ci, ci, ci, ci]
+            L.attn_fwd_ws_bytes.restype = sz
             L.attn_fwd_grouped.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp]
             L.attn_fwd_grouped.restype = ci
             L.attn_fwd_naive.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, cf, ci, ci, vp, sz, vp]
@@ -132,9 +137,18 @@ def _ptr(t):
     return ctypes.c_void_p(0 if t is None else t.data_ptr())
 
 
+def attn_fwd_ws_bytes(B: int, h: int, S: int, d: int, dtype) -> int:
+    """Scratch bytes attn_fwd_ws needs on the current device (0: none)."""
+    return int(lib().attn_fwd_ws_bytes(B, h, S, d, dtype_code(dtype)))
+
+
 def attn_fwd(q, k, v, o=None, lse=None, *, layout: int = LAYOUT_BHSD, scale: float | None = None,
-             want_lse: bool = False, stream=None):
-    """O = softmax(scale·Q·K^T)·V (fused, one launch).  Returns (o, lse or None)."""
+             want_lse: bool = False, stream=None, split: bool = True, workspace=None):
+    """O = softmax(scale·Q·K^T)·V (fused, one launch).  Returns (o, lse or None).
+
+    split=True calls the C entry attn_fwd_ws with a scratch buffer (``workspace``,
+    or one taken from torch's allocator), which lets the kernel cut the last
+    wave of work items along the key axis; split=False calls attn_fwd."""
     torch = _torch()
     B, h, S, d = _dims(q, layout)
     if k.shape != q.shape or v.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
@@ -144,10 +158,25 @@ def attn_fwd(q, k, v, o=None, lse=None, *, layout: int = LAYOUT_BHSD, scale: flo
     if lse is None and want_lse:
         lse = torch.empty((B, h, S), dtype=torch.float32, device=q.device)
     _check_dense(q, k, v, o, lse)
-    rc = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, h, S, d,
-                        float(scale) if scale else 0.0, layout, dtype_code(q.dtype), _stream_ptr(stream))
+    sc = float(scale) if scale else 0.0
+    if not split:
+        rc = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, h, S, d, sc, layout,
+                            dtype_code(q.dtype), _stream_ptr(stream))
+        if rc:
+            raise AttnError(rc, "attn_fwd")
+        return o, lse
+    if workspace is None:
+        need = attn_fwd_ws_bytes(B, h, S, d, q.dtype)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+            if isinstance(stream, torch.cuda.Stream):
+                workspace.record_stream(stream)
+    _check_dense(workspace)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().attn_fwd_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, h, S, d, sc, layout,
+                           dtype_code(q.dtype), _ptr(workspace), nbytes, _stream_ptr(stream))
     if rc:
-        raise AttnError(rc, "attn_fwd")
+        raise AttnError(rc, "attn_fwd_ws")
     return o, lse
 
 

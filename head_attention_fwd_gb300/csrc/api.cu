@@ -6,7 +6,10 @@
 
 #include <math.h>
 #include <stdlib.h>
+#include <unistd.h>
 
+#include <atomic>
+#include <chrono>
 #include <mutex>
 
 #include "attn.h"
@@ -29,6 +32,7 @@ struct DeviceState {
   bool ready = false;
   int rc = ATTN_OK;
   unsigned* status = nullptr;
+  int num_sms = 0;
 };
 
 std::mutex g_mu;
@@ -49,7 +53,9 @@ int device_setup(DeviceState** out) {
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        major != 10 || minor != 3) {
+        major != 10 || minor != 3 ||
+        cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        st.num_sms < 1) {
       st.rc = ATTN_E_DEVICE;
     } else if (cudaGetSymbolAddress(reinterpret_cast<void**>(&st.status), g_status) != cudaSuccess) {
       st.rc = ATTN_E_DEVICE;
@@ -77,6 +83,19 @@ long long wait_limit() {
     return x > 0 ? x : 4000000000LL;
   }();
   return v;
+}
+
+// A tag no earlier launch of this process used (and, seeded from the clock
+// and the process id, unlikely to be one another process left in memory).
+// The pieces of cut items are marked as written with it.
+unsigned long long next_tag() {
+  static std::atomic<unsigned long long> ctr{
+      static_cast<unsigned long long>(std::chrono::steady_clock::now().time_since_epoch().count()) ^
+      (static_cast<unsigned long long>(getpid()) << 40)};
+  unsigned long long z = ctr.fetch_add(0x9e3779b97f4a7c15ULL) + 0x9e3779b97f4a7c15ULL;  // splitmix64
+  z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ULL;
+  z = (z ^ (z >> 27)) * 0x94d049bb133111ebULL;
+  return (z ^ (z >> 31)) | 1ULL;
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -209,9 +228,12 @@ size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 // Flash launch on tensors of a [B,H,S,d] problem; inputs and output may have
 // different row strides (rs_in, rs_out: layout 1 only).  Layout
 // ATTN_LAYOUT_GROUPED takes hg heads per group ([B,H/hg,S,hg,d]).
+// With `scratch` (at least flash_scratch_layout(d, grid).total bytes for the
+// plan's grid) the last waves of items may be cut along the key axis.
 int run_flash(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h, int S,
               int d, float scale, int layout, long long hg, int dtype, long long rs_in,
-              long long rs_out, unsigned* status, cudaStream_t st) {
+              long long rs_out, const DeviceState* ds, cudaStream_t st, void* scratch = nullptr,
+              size_t scratch_bytes = 0) {
   attn::FlashLaunch a;
   int rc = ATTN_OK;
   a.grouped = layout == ATTN_LAYOUT_GROUPED;
@@ -237,9 +259,23 @@ int run_flash(const void* q, const void* k, const void* v, void* o, float* lse, 
   a.B = B, a.H = h, a.S = S, a.d = d;
   a.bf16 = dtype == ATTN_BF16;
   a.scale = scale;
-  a.status = status;
+  a.status = ds->status;
   a.limit = wait_limit();
-  return to_rc(attn::launch_flash_fwd(a, st));
+  a.scratch = nullptr;
+  a.tag = 0;
+  a.clear_flags = false;
+  attn::FlashPlan plan = attn::plan_flash(B, h, S, d, ds->num_sms, scratch != nullptr);
+  if (plan.sk_units > 0) {
+    if (scratch_bytes < attn::flash_scratch_layout(d, plan.grid).total) return ATTN_E_WORKSPACE;
+    a.scratch = scratch;
+    a.tag = next_tag();
+    // A captured launch replays with the same tag: its flags must start clear.
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(st, &cs);
+    if (e != cudaSuccess) return to_rc(e);
+    a.clear_flags = cs != cudaStreamCaptureStatusNone;
+  }
+  return to_rc(attn::launch_flash_fwd(a, plan, st));
 }
 
 }  // namespace
@@ -269,7 +305,39 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
     return to_rc(attn::launch_simt_fwd(a, st));
   }
   const long long rs = static_cast<long long>(h) * d;
-  return run_flash(q, k, v, o, lse, B, h, S, d, sc, layout, 1, dtype, rs, rs, ds->status, st);
+  return run_flash(q, k, v, o, lse, B, h, S, d, sc, layout, 1, dtype, rs, rs, ds, st);
+}
+
+size_t attn_fwd_ws_bytes(int B, int h, int S, int d, int dtype) {
+  if (B < 1 || h < 1 || S < 1 || (dtype != ATTN_F16 && dtype != ATTN_BF16) || (d != 64 && d != 128))
+    return 0;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    return 0;
+  const attn::FlashPlan plan = attn::plan_flash(B, h, S, d, sms, true);
+  return plan.sk_units > 0 ? attn::flash_scratch_layout(d, plan.grid).total : 0;
+}
+
+int attn_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h,
+                int S, int d, float scale, int layout, int dtype, void* workspace, size_t ws_bytes,
+                void* stream) {
+  int rc = validate_attn(q, k, v, o, lse, B, h, S, d, layout, dtype);
+  if (rc) return rc;
+  if (dtype == ATTN_F32 || (!workspace && ws_bytes == 0))
+    return attn_fwd(q, k, v, o, lse, B, h, S, d, scale, layout, dtype, stream);
+  if (!workspace || !aligned(workspace, 256)) return ATTN_E_WORKSPACE;
+  const size_t bytes = static_cast<size_t>(B) * h * S * d * 2;
+  if (overlap(workspace, ws_bytes, q, bytes) || overlap(workspace, ws_bytes, k, bytes) ||
+      overlap(workspace, ws_bytes, v, bytes) || overlap(workspace, ws_bytes, o, bytes) ||
+      (lse && overlap(workspace, ws_bytes, lse, static_cast<size_t>(B) * h * S * 4)))
+    return ATTN_E_ALIAS;
+  DeviceState* ds = nullptr;
+  if ((rc = device_setup(&ds))) return rc;
+  const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(d));
+  const long long rs = static_cast<long long>(h) * d;
+  return run_flash(q, k, v, o, lse, B, h, S, d, sc, layout, 1, dtype, rs, rs, ds,
+                   static_cast<cudaStream_t>(stream), workspace, ws_bytes);
 }
 
 int attn_fwd_grouped(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h,
@@ -283,7 +351,7 @@ int attn_fwd_grouped(const void* q, const void* k, const void* v, void* o, float
   const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(d));
   const long long rs = static_cast<long long>(h) * d;
   return run_flash(q, k, v, o, lse, B, h, S, d, sc, ATTN_LAYOUT_GROUPED, heads_per_group, dtype, rs,
-                   rs, ds->status, static_cast<cudaStream_t>(stream));
+                   rs, ds, static_cast<cudaStream_t>(stream));
 }
 
 size_t attn_fwd_naive_workspace_bytes(int B, int h, int S, int dtype) {
@@ -427,7 +495,7 @@ int qkv_proj_attn(const void* x, const void* w_qkv, void* o, int B, int S, int D
   const uint8_t* base = static_cast<const uint8_t*>(workspace);
   return run_flash(base, base + static_cast<size_t>(D) * 2, base + static_cast<size_t>(2 * D) * 2, o,
                    nullptr, B, h, S, d, 1.0f / sqrtf(static_cast<float>(d)), ATTN_LAYOUT_BSHD, 1,
-                   dtype, 3LL * D, D, ds->status, st);
+                   dtype, 3LL * D, D, ds, st);
 }
 
 const char* attn_status_string(int status) {

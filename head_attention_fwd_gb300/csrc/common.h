@@ -26,8 +26,35 @@ struct FlashLaunch {
   float scale;                  // softmax scale (already resolved)
   unsigned* status;             // device status word
   long long limit;              // clock cycles per wait before giving up
+  void* scratch;                // pieces of cut items (plan.sk_units > 0), flash_scratch_layout bytes
+  unsigned long long tag;       // unique per launch: marks this launch's pieces as written
+  bool clear_flags;             // zero the piece flags first (needed when the launch can be replayed)
 };
-cudaError_t launch_flash_fwd(const FlashLaunch& a, cudaStream_t st);
+
+// Work list of the persistent attention kernel.  An item is one (batch, head)
+// and 256 query rows; items [0, dp_end) run whole, item i on CTA i % grid;
+// the sk_units key tiles of the remaining items are cut into equal runs, CTA
+// g taking units [g·sk_units/grid, (g+1)·sk_units/grid).
+struct FlashPlan {
+  int mode;                     // 0: one item per CTA; 1: persistent, whole items; 2: persistent + cut
+  int grid;
+  int n_qblk, n_kv;             // items per (batch, head); key tiles per item
+  long long dp_end;
+  long long sk_units;           // 0: no item is cut, no scratch is used
+};
+// split = false: whole items only.  split = true: cut the last one to two
+// waves (only when the item count is not a multiple of num_sms).  The mode
+// also depends on the head dimension d.
+FlashPlan plan_flash(int B, int H, int S, int d, int num_sms, bool split);
+
+// Scratch of a plan with cut items: per CTA 8 flags, then (m, l) and the
+// unnormalised O of 256 rows.
+struct FlashScratch {
+  size_t off_flags, flag_bytes, off_ml, off_opart, total;
+};
+FlashScratch flash_scratch_layout(int d, int grid);
+
+cudaError_t launch_flash_fwd(const FlashLaunch& a, const FlashPlan& plan, cudaStream_t st);
 
 struct SimtLaunch {
   const float *q, *k, *v;

@@ -65,8 +65,8 @@ __device__ __forceinline__ void raise_abort(const WaitCtx& w, uint32_t code) {
 
 // With honor_abort = false the wait ignores the abort flag (used to drain
 // copies and MMAs already in flight before a CTA winds down).
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtx& w,
-                                            uint32_t code, bool honor_abort = true) {
+__device__ __forceinline__ bool mbar_wait_loop(uint32_t bar, uint32_t parity, const WaitCtx& w,
+                                               uint32_t code, bool honor_abort = true) {
   const long long t0 = clock64();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -79,20 +79,61 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
     }
   }
 }
+// The same loop out of line, to keep it out of hot code (INL = false), or
+// inline where a kernel must call no functions (INL = true).
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtx& w,
+                                                   uint32_t code, bool honor_abort = true) {
+  return mbar_wait_loop(bar, parity, w, code, honor_abort);
+}
 
 // Bounded wait for the phase with the given parity to complete.
+template <bool INL = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtx& w,
                                           uint32_t code) {
   if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, w, code);
+  if constexpr (INL)
+    return mbar_wait_loop(bar, parity, w, code);
+  else
+    return mbar_wait_slow(bar, parity, w, code);
 }
 
 // Same, with the outcome made uniform over the calling warp (every lane must
 // call it): false on every lane if any lane gave up.
+template <bool INL = false>
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const WaitCtx& w,
                                                uint32_t code) {
-  const bool ok = mbar_wait(bar, parity, w, code);
+  const bool ok = mbar_wait<INL>(bar, parity, w, code);
   return __all_sync(0xffffffffu, ok);
+}
+
+// ------------------------------------------- flags between CTAs (global) ----
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Bounded wait of a whole warp until *f == tag.  Every lane polls with an
+// acquire load, so every lane is ordered after the writer's release.  Gives
+// up (false on every lane) when the CTA aborts or after w.limit cycles, in
+// which case `code` is recorded.
+__device__ __forceinline__ bool flag_wait_warp(const unsigned long long* f, unsigned long long tag,
+                                               const WaitCtx& w, uint32_t code) {
+  const long long t0 = clock64();
+  for (uint32_t n = 1;; ++n) {
+    if (__all_sync(0xffffffffu, ld_acquire_u64(f) == tag)) return true;
+    if ((n & 15u) == 0) {
+      const bool late = __shfl_sync(0xffffffffu, clock64() - t0 > w.limit ? 1 : 0, 0) != 0;
+      if (late || __any_sync(0xffffffffu, *w.abort_flag != 0)) {
+        if (late && (threadIdx.x & 31u) == 0) raise_abort(w, code);
+        return false;
+      }
+    }
+    __nanosleep(64);
+  }
 }
 
 // ----------------------------------------------------------------- TMA ----

@@ -89,6 +89,43 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
              int d, float scale, int layout, int dtype, void* stream);
 
 /*
+ * attn_fwd_ws -- attn_fwd with a caller scratch buffer that lets the kernel
+ * balance the last wave.  The work items are (batch, head, 256 query rows);
+ * attn_fwd deals whole items to at most one CTA per SM, so when the item
+ * count is not a multiple of the SM count the last wave leaves SMs idle.
+ * With the scratch, the last one to two waves of items are cut along the key
+ * axis into equal runs of 128-key tiles, one run per SM.  Each later piece of
+ * a cut item leaves its running max m, exp-sum l and unnormalised output in
+ * the scratch; the piece that starts at key 0 merges them into its own with
+ * the merge rule of "Transformer算子生态深度分析" §2.6 (each side rescaled by
+ * exp(m_side - m), then added), the rule that also merges consecutive key
+ * tiles.  The result equals attn_fwd's up to fp32 rounding order.
+ *
+ *   workspace  [in/out] device scratch of at least
+ *              attn_fwd_ws_bytes(B, h, S, d, dtype) bytes, 256-byte aligned,
+ *              owned by the caller and used by this call until the stream
+ *              reaches it; its contents on entry do not matter.  NULL with
+ *              ws_bytes = 0 runs attn_fwd.
+ *   other arguments, lse and layouts as attn_fwd.  ATTN_F32 ignores the
+ *   workspace (the fp32 path has no waves to balance).
+ *
+ * Errors: as attn_fwd, plus ATTN_E_WORKSPACE (misaligned, or smaller than
+ * attn_fwd_ws_bytes for the current device) and ATTN_E_ALIAS (workspace
+ * overlaps a tensor).
+ */
+int attn_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h,
+                int S, int d, float scale, int layout, int dtype, void* workspace, size_t ws_bytes,
+                void* stream);
+
+/*
+ * Scratch bytes attn_fwd_ws needs on the current device (it depends on the
+ * SM count): per SM 64 bytes of flags and 256 rows of (m, l) and d fp32
+ * values.  0 when no item would be cut (the item count is a multiple of the
+ * SM count), for ATTN_F32, for unsupported sizes, or without a device.
+ */
+size_t attn_fwd_ws_bytes(int B, int h, int S, int d, int dtype);
+
+/*
  * attn_fwd_grouped -- attn_fwd on the third layout of "WebGPU 算子优化：QKV
  * 内存合并与 FlashAttention 分块计算", §QKV 矩阵的内存合并模式选择 ("split":
  * heads in groups, each group stored contiguously).  q, k, v, o are

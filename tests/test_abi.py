@@ -87,6 +87,29 @@ def test_valid_call_without_gpu_reports_device_error(L):
     assert fwd(L) == E["DEVICE"]
 
 
+def test_attn_fwd_ws_validation(L):
+    vp = ctypes.c_void_p
+    WS = 64 * A
+
+    def fwd_ws(ws=WS, nbytes=1 << 24, dtype=1, o=O, d=64):
+        return L.attn_fwd_ws(vp(Q), vp(K), vp(V), vp(o), vp(None), 1, 16, 4096, d, 0.0, 0, dtype, vp(ws),
+                             nbytes, vp(0))
+
+    assert fwd_ws(o=None) == E["NULL"]
+    assert fwd_ws(d=96) == E["SHAPE"]
+    assert fwd_ws(ws=WS + 128) == E["WORKSPACE"]      # not 256-byte aligned
+    assert fwd_ws(ws=None, nbytes=64) == E["WORKSPACE"]
+    assert fwd_ws(ws=Q) == E["ALIAS"]
+    assert fwd_ws(ws=O - 1024) == E["ALIAS"]
+    assert L.attn_fwd_ws_bytes(1, 16, 4096, 64, 0) == 0   # fp32: no scratch
+    assert L.attn_fwd_ws_bytes(1, 16, 4096, 96, 1) == 0   # unsupported d
+    assert L.attn_fwd_ws_bytes(0, 16, 4096, 64, 1) == 0
+    if not torch.cuda.is_available():
+        assert L.attn_fwd_ws_bytes(1, 16, 4096, 64, 1) == 0  # depends on the device's SM count
+        assert fwd_ws() == E["DEVICE"]
+        assert fwd_ws(ws=None, nbytes=0) == E["DEVICE"]      # plain attn_fwd
+
+
 def test_naive_validation_and_workspace(L):
     vp = ctypes.c_void_p
     need = L.attn_fwd_naive_workspace_bytes(1, 16, 4096, 1)

@@ -40,14 +40,90 @@ SHAPES16 = [(1, 1, 1, 64), (1, 2, 128, 64), (2, 3, 300, 64), (1, 1, 513, 64), (1
 @pytest.mark.parametrize("shape", SHAPES16, ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("layout", [0, 1])
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
-def test_flash_matches_oracle(dev, shape, layout, dtype):
+@pytest.mark.parametrize("split", [True, False], ids=["split", "whole"])
+def test_flash_matches_oracle(dev, shape, layout, dtype, split):
+    """split: items cut along the key axis over the SMs (at these sizes every
+    item is cut into pieces of one or a few key tiles); whole: attn_fwd."""
     B, h, S, d = shape
     q, k, v = rand_qkv(B, h, S, d, dtype, layout, seed=hash(shape) % 10000 + layout)
-    o, lse = attn.attn_fwd(q.to(dev), k.to(dev), v.to(dev), layout=layout, want_lse=True)
+    o, lse = attn.attn_fwd(q.to(dev), k.to(dev), v.to(dev), layout=layout, want_lse=True, split=split)
     device_status_ok()
     o_ref, lse_ref = oracle.attention(q, k, v, layout=layout, scale=1 / math.sqrt(d))
     check_o(o, o_ref, dtype, f"flash {shape} L{layout}")
     check_lse(lse, lse_ref, f"flash {shape} L{layout}")
+
+
+# More work items (B·h·ceil(S/256)) than SMs: CTAs run several items in turn,
+# and with a scratch the last one to two waves are cut along the key axis.
+PERSISTENT = [(1, 80, 512, 64), (2, 41, 300, 64), (1, 77, 640, 128), (1, 160, 256, 128)]
+
+
+@pytest.mark.parametrize("shape", PERSISTENT, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("split", [True, False], ids=["split", "whole"])
+def test_flash_persistent_schedule_matches_oracle(dev, shape, split):
+    B, h, S, d = shape
+    dtype = torch.bfloat16 if d == 128 else torch.float16
+    q, k, v = rand_qkv(B, h, S, d, dtype, 0, seed=h * S + d)
+    o, lse = attn.attn_fwd(q.to(dev), k.to(dev), v.to(dev), want_lse=True, split=split)
+    device_status_ok()
+    o_ref, lse_ref = oracle.attention(q, k, v, scale=1 / math.sqrt(d))
+    check_o(o, o_ref, dtype, f"persistent {shape}")
+    check_lse(lse, lse_ref, f"persistent {shape}")
+
+
+def test_split_and_whole_agree(dev):
+    """The cut-and-merge schedule and the whole-item schedule give the same
+    result up to fp32 summation order (one 16-bit rounding step apart at most)."""
+    q, k, v = (t.to(dev) for t in rand_qkv(1, 16, 4096, 64, torch.float16, 0, seed=7))
+    assert attn.attn_fwd_ws_bytes(1, 16, 4096, 64, torch.float16) > 0  # 256 items: not a multiple of the SMs
+    o1, l1 = attn.attn_fwd(q, k, v, want_lse=True, split=True)
+    o2, l2 = attn.attn_fwd(q, k, v, want_lse=True, split=False)
+    device_status_ok()
+    d = (o1.float() - o2.float()).abs()
+    assert d.max().item() <= 2e-3 and d.mean().item() <= 1e-4
+    assert (l1 - l2).abs().max().item() <= 1e-4
+
+
+def test_split_workspace_too_small_is_rejected(dev):
+    import ctypes
+    q, k, v = (t.to(dev) for t in rand_qkv(1, 16, 1024, 64, torch.float16, 0, seed=8))
+    o = torch.empty_like(q)
+    need = attn.attn_fwd_ws_bytes(1, 16, 1024, 64, torch.float16)
+    assert need > 0
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    vp = ctypes.c_void_p
+    L = attn.lib()
+    args = [vp(q.data_ptr()), vp(k.data_ptr()), vp(v.data_ptr()), vp(o.data_ptr()), None, 1, 16, 1024, 64,
+            0.0, 0, 1]
+    assert L.attn_fwd_ws(*args, vp(ws.data_ptr()), need - 256, vp(0)) == -6
+    assert L.attn_fwd_ws(*args, vp(ws.data_ptr() + 128), need - 256, vp(0)) == -6
+    assert L.attn_fwd_ws(*args, vp(ws.data_ptr()), need, vp(0)) == 0
+    device_status_ok()
+
+
+def test_split_schedule_replays_in_a_cuda_graph(dev):
+    """A captured split launch replays with a fixed tag; its piece flags are
+    cleared inside the graph, so every replay waits for its own pieces."""
+    B, h, S, d = 1, 24, 700, 64
+    qs, ks, vs = (torch.empty((B, h, S, d), dtype=torch.float16, device=dev) for _ in range(3))
+    os_ = torch.empty_like(qs)
+    ws = torch.empty(attn.attn_fwd_ws_bytes(B, h, S, d, torch.float16), dtype=torch.uint8, device=dev)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # warm-up outside the capture
+        attn.attn_fwd(qs, ks, vs, os_, workspace=ws)
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        attn.attn_fwd(qs, ks, vs, os_, workspace=ws)
+    for seed in (1, 2, 3):
+        q, k, v = rand_qkv(B, h, S, d, torch.float16, 0, seed=100 + seed)
+        qs.copy_(q), ks.copy_(k), vs.copy_(v)
+        g.replay()
+        torch.cuda.synchronize()
+        device_status_ok()
+        o_eager, _ = attn.attn_fwd(qs, ks, vs, split=True)
+        assert torch.equal(os_, o_eager)
 
 
 @pytest.mark.parametrize("d", [64, 128])

@@ -28,7 +28,8 @@ def test_auto_runs_the_selected_kernel(dev, opt, S, want):
     o, _, kind = attn.attn_fwd_auto(q, k, v, option_enabled=opt)
     device_status_ok()
     assert kind == want
-    ref = attn.attn_fwd(q, k, v)[0] if want == attn.ATTN_KERNEL_ONLINE else attn.attn_fwd_naive(q, k, v)[0]
+    ref = (attn.attn_fwd(q, k, v, split=False)[0] if want == attn.ATTN_KERNEL_ONLINE
+           else attn.attn_fwd_naive(q, k, v)[0])
     device_status_ok()
     assert torch.equal(o, ref)
 

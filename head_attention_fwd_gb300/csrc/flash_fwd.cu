@@ -278,17 +278,23 @@ __global__ void __launch_bounds__(352, 1)
       mbar_init(bar(C::bar_ofree(t)), 128);
     }
     if constexpr (MODE != MODE_ONE) cta_work_init(p, work);
-    // A CTA that starts after another one gave up does no work.
-    *abort_flag = (*reinterpret_cast<volatile unsigned*>(p.status) != 0u) ? 1 : 0;
-    fence_mbar_init();
   }
   if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
+  // The set-up above overlaps the previous grid's tail; global memory is
+  // touched only after it has completed.
+  griddep_wait();
+  if (threadIdx.x == 0) {
+    // A CTA that starts after another one gave up does no work.
+    *abort_flag = (*reinterpret_cast<volatile unsigned*>(p.status) != 0u) ? 1 : 0;
+    fence_mbar_init();
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  griddep_launch_dependents();
   const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_slot, 0);
   const WaitCtx wc{abort_flag, p.status, p.limit};
   const bool skip = *abort_flag != 0;
@@ -905,7 +911,20 @@ cudaError_t launch_impl(const FlashLaunch& a, const FlashPlan& plan, cudaStream_
       if (e != cudaSuccess) return e;
     }
   }
-  kern<<<static_cast<unsigned>(plan.grid), C::THREADS, C::SMEM, st>>>(a.tq, a.tk, a.tv, p);
+  // Launched as a programmatic dependent of the previous work in the stream:
+  // the kernel waits (griddepcontrol.wait) before its first global access.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(plan.grid));
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, a.tq, a.tk, a.tv, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -106,6 +106,14 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, co
   return __all_sync(0xffffffffu, ok);
 }
 
+// Programmatic dependent launch: wait until the grids this one depends on
+// have completed and their memory is visible; let the next grid in the
+// stream start launching its CTAs (they take SMs only as this grid's leave).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------- flags between CTAs (global) ----
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
   unsigned long long v;

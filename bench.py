@@ -417,6 +417,20 @@ def run_extra(attn, w, sets, stream, dev):
     t = time_launches(lambda i: attn.attn_fwd(*sets[i % N_SETS], layout=w.layout, stream=stream,
                                               split=False), n, stream)
     out[w.name + "_whole_items"] = {"tflops": w.attn_flops * n / t / 1e12, "ms": t / n * 1e3}
+    # fp32 inputs, fp16 output: one conversion launch, then the fused kernel
+    q32, k32, v32 = (x.float() for x in (q, k, v))
+    wsm = torch.empty(attn.attn_fwd_mixed_workspace_bytes(w.B, w.h, w.S, w.d, q.dtype), dtype=torch.uint8,
+                      device=dev)
+    for _ in range(3):
+        attn.attn_fwd_mixed(q32, k32, v32, o, workspace=wsm, out_dtype=q.dtype, layout=w.layout, stream=stream)
+    n = 200
+    t = time_launches(lambda i: attn.attn_fwd_mixed(q32, k32, v32, o, workspace=wsm, out_dtype=q.dtype,
+                                                    layout=w.layout, stream=stream), n, stream)
+    conv_bytes = 3 * q.numel() * (4 + 2)
+    out["mixed_f32_in_" + w.name] = {"tflops": w.attn_flops * n / t / 1e12, "ms": t / n * 1e3,
+                                     "launches_per_call": 2,
+                                     "conversion_bytes": conv_bytes}
+    del q32, k32, v32, wsm
     for name in ("long_seq_bf16_peaky", "wide_head_bf16_bshd"):
         ww = WORKLOADS[name]
         g = torch.Generator(device=dev).manual_seed(ww.seed)

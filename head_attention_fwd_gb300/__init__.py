@@ -9,6 +9,7 @@ Entry points (same names as the C ABI):
 
 * ``attn_fwd(q, k, v, ...)``        fused online-softmax attention (through
   ``attn_fwd_ws`` with a small scratch unless ``split=False``)
+* ``attn_fwd_mixed(q, k, v, ...)``  fp32 inputs, 16-bit output (converted once, then fused)
 * ``attn_fwd_naive(q, k, v, ...)``  unfused two-pass-softmax comparison path
 * ``qkv_proj_attn(x, w_qkv, h, ...)`` fused QKV projection, then attention
 * ``qkv_proj_attn_noalloc(x, w_qkv, h, ...)`` the same without a workspace argument
@@ -60,6 +61,10 @@ def lib() -> ctypes.CDLL:
             L.attn_fwd_ws.restype = ci
             L.attn_fwd_ws_bytes.argtypes = [ci, ci, ci, ci, ci]
             L.attn_fwd_ws_bytes.restype = sz
+            L.attn_fwd_mixed.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, cf, ci, ci, vp, sz, vp]
+            L.attn_fwd_mixed.restype = ci
+            L.attn_fwd_mixed_workspace_bytes.argtypes = [ci, ci, ci, ci, ci]
+            L.attn_fwd_mixed_workspace_bytes.restype = sz
             L.attn_fwd_grouped.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp]
             L.attn_fwd_grouped.restype = ci
             L.attn_fwd_naive.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, cf, ci, ci, vp, sz, vp]
@@ -178,6 +183,38 @@ def attn_fwd(q, k, v, o=None, lse=None, *, layout: int = LAYOUT_BHSD, scale: flo
     if rc:
         raise AttnError(rc, "attn_fwd_ws")
     return o, lse
+
+
+def attn_fwd_mixed_workspace_bytes(B: int, h: int, S: int, d: int, out_dtype) -> int:
+    return int(lib().attn_fwd_mixed_workspace_bytes(B, h, S, d, dtype_code(out_dtype)))
+
+
+def attn_fwd_mixed(q, k, v, o=None, lse=None, workspace=None, *, out_dtype=None, layout: int = LAYOUT_BHSD,
+                   scale: float | None = None, want_lse: bool = False, stream=None):
+    """fp32 q, k, v -> 16-bit o (out_dtype, default float16).  Returns (o, lse or None, workspace)."""
+    torch = _torch()
+    out_dtype = out_dtype or torch.float16
+    B, h, S, d = _dims(q, layout)
+    if q.dtype != torch.float32 or k.dtype != torch.float32 or v.dtype != torch.float32:
+        raise ValueError("q, k, v must be float32")
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must share one shape")
+    if o is None:
+        o = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, h, S), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(attn_fwd_mixed_workspace_bytes(B, h, S, d, out_dtype), dtype=torch.uint8,
+                                device=q.device)
+        if isinstance(stream, torch.cuda.Stream):
+            workspace.record_stream(stream)
+    _check_dense(q, k, v, o, lse, workspace)
+    rc = lib().attn_fwd_mixed(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, h, S, d,
+                              float(scale) if scale else 0.0, layout, dtype_code(o.dtype), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    if rc:
+        raise AttnError(rc, "attn_fwd_mixed")
+    return o, lse, workspace
 
 
 def attn_fwd_grouped(q, k, v, o=None, lse=None, *, scale: float | None = None, want_lse: bool = False,

@@ -340,6 +340,63 @@ int attn_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse
                    static_cast<cudaStream_t>(stream), workspace, ws_bytes);
 }
 
+size_t attn_fwd_mixed_workspace_bytes(int B, int h, int S, int d, int out_dtype) {
+  if (B < 1 || h < 1 || S < 1 || (out_dtype != ATTN_F16 && out_dtype != ATTN_BF16) || (d != 64 && d != 128))
+    return 0;
+  const long long n = static_cast<long long>(B) * h * S * d;
+  if (n > (1LL << 40)) return 0;
+  return 3 * round256(static_cast<size_t>(n) * 2) + attn_fwd_ws_bytes(B, h, S, d, out_dtype);
+}
+
+int attn_fwd_mixed(const float* q, const float* k, const float* v, void* o, float* lse, int B, int h,
+                   int S, int d, float scale, int layout, int out_dtype, void* workspace, size_t ws_bytes,
+                   void* stream) {
+  if (!q || !k || !v || !o) return ATTN_E_NULL;
+  if (layout != ATTN_LAYOUT_BHSD && layout != ATTN_LAYOUT_BSHD) return ATTN_E_LAYOUT;
+  if (out_dtype != ATTN_F16 && out_dtype != ATTN_BF16) return ATTN_E_DTYPE;
+  if (B < 1 || h < 1 || S < 1 || (d != 64 && d != 128)) return ATTN_E_SHAPE;
+  const long long n = static_cast<long long>(B) * h * S * d;
+  if (n > (1LL << 40) || static_cast<long long>(B) * h * ((S + 255) / 256) > 0x7fffffffLL) return ATTN_E_SHAPE;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || (lse && !aligned(lse, 4)))
+    return ATTN_E_ALIGN;
+  const size_t in_b = static_cast<size_t>(n) * 4, out_b = static_cast<size_t>(n) * 2;
+  const size_t lse_b = static_cast<size_t>(B) * h * S * 4;
+  if (overlap(o, out_b, q, in_b) || overlap(o, out_b, k, in_b) || overlap(o, out_b, v, in_b) ||
+      (lse && (overlap(lse, lse_b, q, in_b) || overlap(lse, lse_b, k, in_b) || overlap(lse, lse_b, v, in_b) ||
+               overlap(lse, lse_b, o, out_b))))
+    return ATTN_E_ALIAS;
+  const size_t conv = 3 * round256(out_b);
+  if (!workspace || !aligned(workspace, 256) || ws_bytes < conv) return ATTN_E_WORKSPACE;
+  if (overlap(workspace, ws_bytes, q, in_b) || overlap(workspace, ws_bytes, k, in_b) ||
+      overlap(workspace, ws_bytes, v, in_b) || overlap(workspace, ws_bytes, o, out_b) ||
+      (lse && overlap(workspace, ws_bytes, lse, lse_b)))
+    return ATTN_E_ALIAS;
+  DeviceState* ds = nullptr;
+  int rc = device_setup(&ds);
+  if (rc) return rc;
+  // Scratch beyond the three copies, if any, must hold the whole cut-wave
+  // scratch: checked before the first launch.
+  const size_t rest = ws_bytes - conv;
+  if (rest > 0) {
+    const attn::FlashPlan plan = attn::plan_flash(B, h, S, d, ds->num_sms, true);
+    if (plan.sk_units > 0 && rest < attn::flash_scratch_layout(d, plan.grid).total) return ATTN_E_WORKSPACE;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  attn::ConvertLaunch cv;
+  cv.q = q, cv.k = k, cv.v = v;
+  cv.out = reinterpret_cast<uint16_t*>(ws);
+  cv.n = n;
+  cv.out_stride = static_cast<long long>(round256(out_b) / 2);
+  cv.bf16 = out_dtype == ATTN_BF16;
+  cv.num_sms = ds->num_sms;
+  if ((rc = to_rc(attn::launch_convert3(cv, st)))) return rc;
+  const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(d));
+  const long long rs = static_cast<long long>(h) * d;
+  return run_flash(ws, ws + round256(out_b), ws + 2 * round256(out_b), o, lse, B, h, S, d, sc, layout, 1,
+                   out_dtype, rs, rs, ds, st, rest > 0 ? ws + conv : nullptr, rest);
+}
+
 int attn_fwd_grouped(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h,
                      int S, int d, int heads_per_group, float scale, int dtype, void* stream) {
   int rc = validate_attn(q, k, v, o, lse, B, h, S, d, ATTN_LAYOUT_BHSD, dtype);

@@ -88,6 +88,18 @@ struct GemmLaunch {
 };
 cudaError_t launch_gemm(const GemmLaunch& a, cudaStream_t st);
 
+// fp32 -> 16-bit copies of Q, K, V (attn_fwd_mixed): out[i·out_stride + j] =
+// round_to_nearest(src_i[j]) for the three tensors, n elements each (n % 8 == 0,
+// all pointers 16-byte aligned).
+struct ConvertLaunch {
+  const float *q, *k, *v;
+  uint16_t* out;
+  long long n, out_stride;      // elements per tensor; element offset between the outputs
+  bool bf16;
+  int num_sms;
+};
+cudaError_t launch_convert3(const ConvertLaunch& a, cudaStream_t st);
+
 // Naive softmax passes over an fp32 score matrix [rows, n] (row stride ld):
 //   pass 1: stats[r] = (max_j S[r,j], sum_j exp(S[r,j] - max))
 //   pass 2: P[r,j] = exp(S[r,j] - m_r) / l_r  (16-bit), and lse[...] if asked

@@ -126,6 +126,36 @@ int attn_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse
 size_t attn_fwd_ws_bytes(int B, int h, int S, int d, int dtype);
 
 /*
+ * attn_fwd_mixed -- fp32 inputs, 16-bit output: the mixed-precision split of
+ * "WebGPU 算子优化：QKV 内存合并与 FlashAttention 分块计算",
+ * §浏览器端落地的关键参数与监控 (16-bit score products, fp32 softmax
+ * statistics, 16-bit output) for callers that hold Q, K, V in fp32.
+ *
+ *   q, k, v    [in]  fp32, B·h·S·d elements each, in `layout`.
+ *   o          [out] `out_dtype` (ATTN_F16 or ATTN_BF16), same shape and layout.
+ *   lse        [out] optional fp32 [B, h, S].
+ *   workspace  device scratch, 256-byte aligned, of
+ *              attn_fwd_mixed_workspace_bytes(B, h, S, d, out_dtype) bytes or
+ *              more; exactly 3·round_up(B·h·S·d·2, 256) bytes skips the
+ *              last-wave balancing of attn_fwd_ws, and a size in between is
+ *              rejected.  On return it holds the rounded copies of q, k, v,
+ *              in that order, each at a 256-byte aligned offset.
+ *   other arguments as attn_fwd; d in {64, 128}.
+ *
+ * Two launches on `stream`: one conversion kernel rounds q, k, v to
+ * out_dtype (round to nearest even; fp16 overflows to inf above 65504), then
+ * the fused kernel runs on the copies as attn_fwd_ws does.  Errors:
+ * ATTN_E_NULL, ATTN_E_LAYOUT, ATTN_E_DTYPE (out_dtype), ATTN_E_SHAPE,
+ * ATTN_E_ALIGN, ATTN_E_ALIAS, ATTN_E_WORKSPACE, ATTN_E_DEVICE, or a cudaError_t.
+ */
+int attn_fwd_mixed(const float* q, const float* k, const float* v, void* o, float* lse, int B, int h,
+                   int S, int d, float scale, int layout, int out_dtype, void* workspace, size_t ws_bytes,
+                   void* stream);
+
+/* Workspace bytes attn_fwd_mixed needs on the current device (0 for invalid sizes). */
+size_t attn_fwd_mixed_workspace_bytes(int B, int h, int S, int d, int out_dtype);
+
+/*
  * attn_fwd_grouped -- attn_fwd on the third layout of "WebGPU 算子优化：QKV
  * 内存合并与 FlashAttention 分块计算", §QKV 矩阵的内存合并模式选择 ("split":
  * heads in groups, each group stored contiguously).  q, k, v, o are

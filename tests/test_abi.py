@@ -110,6 +110,36 @@ def test_attn_fwd_ws_validation(L):
         assert fwd_ws(ws=None, nbytes=0) == E["DEVICE"]      # plain attn_fwd
 
 
+def test_attn_fwd_mixed_validation_and_workspace(L):
+    vp = ctypes.c_void_p
+    n = 1 * 16 * 4096 * 64
+    copies = 3 * ((n * 2 + 255) // 256 * 256)
+    need = L.attn_fwd_mixed_workspace_bytes(1, 16, 4096, 64, 1)
+    assert need >= copies
+    if not torch.cuda.is_available():
+        assert need == copies                       # no device: no balancing scratch counted
+    assert L.attn_fwd_mixed_workspace_bytes(1, 16, 4096, 64, 0) == 0   # output must be 16-bit
+    assert L.attn_fwd_mixed_workspace_bytes(1, 16, 4096, 96, 1) == 0
+    WS = 64 * A
+
+    def mixed(q=Q, o=O, ws=WS, nbytes=copies, out=1, d=64, layout=0):
+        return L.attn_fwd_mixed(vp(q), vp(K), vp(V), vp(o), vp(None), 1, 16, 4096, d, 0.0, layout, out,
+                                vp(ws), nbytes, vp(0))
+
+    assert mixed(q=None) == E["NULL"]
+    assert mixed(out=0) == E["DTYPE"]
+    assert mixed(d=32) == E["SHAPE"]
+    assert mixed(layout=2) == E["LAYOUT"]
+    assert mixed(q=Q + 4) == E["ALIGN"]
+    assert mixed(o=Q + 1024) == E["ALIAS"]          # the 16-bit output inside the fp32 input
+    assert mixed(ws=None) == E["WORKSPACE"]
+    assert mixed(nbytes=copies - 256) == E["WORKSPACE"]
+    assert mixed(ws=WS + 64) == E["WORKSPACE"]
+    assert mixed(ws=K) == E["ALIAS"]
+    if not torch.cuda.is_available():
+        assert mixed() == E["DEVICE"]
+
+
 def test_naive_validation_and_workspace(L):
     vp = ctypes.c_void_p
     need = L.attn_fwd_naive_workspace_bytes(1, 16, 4096, 1)

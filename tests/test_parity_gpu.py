@@ -257,3 +257,31 @@ def test_grouped_layout_rejects_bad_groups(dev):
     p, po = vp(q.data_ptr()), vp(o.data_ptr())
     assert L.attn_fwd_grouped(p, p, p, po, None, 1, 6, 64, 64, 4, 0.0, 1, vp(0)) == -2  # 4 does not divide 6
     assert L.attn_fwd_grouped(p, p, p, po, None, 1, 6, 64, 64, 3, 0.0, 0, vp(0)) == -5  # fp32: not supported
+
+
+MIXED = [(1, 2, 300, 64), (2, 3, 129, 128), (1, 20, 512, 64)]
+
+
+@pytest.mark.parametrize("shape", MIXED, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("layout", [0, 1])
+@pytest.mark.parametrize("out_dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
+def test_mixed_fp32_inputs_match_oracle(dev, shape, layout, out_dtype):
+    """fp32 Q, K, V -> 16-bit O: against the oracle on the fp32 values, and bit-identical to
+    attn_fwd_ws on the inputs rounded to the output type (the conversion rounds to nearest even)."""
+    B, h, S, d = shape
+    q, k, v = rand_qkv(B, h, S, d, torch.float32, layout, seed=S + d + layout)
+    o, lse, ws = attn.attn_fwd_mixed(q.to(dev), k.to(dev), v.to(dev), out_dtype=out_dtype, layout=layout,
+                                     want_lse=True)
+    device_status_ok()
+    assert o.dtype == out_dtype
+    o_ref, lse_ref = oracle.attention(q, k, v, layout=layout, scale=1 / math.sqrt(d))
+    check_o(o, o_ref, out_dtype, f"mixed {shape}")
+    check_lse(lse, lse_ref, f"mixed {shape}")
+    o16, lse16 = attn.attn_fwd(q.to(out_dtype).to(dev), k.to(out_dtype).to(dev), v.to(out_dtype).to(dev),
+                               layout=layout, want_lse=True)
+    device_status_ok()
+    assert torch.equal(o, o16) and torch.equal(lse, lse16)
+    n = B * h * S * d
+    off = (n * 2 + 255) // 256 * 256
+    assert torch.equal(ws[:n * 2].view(out_dtype).cpu(), q.to(out_dtype).reshape(-1))
+    assert torch.equal(ws[2 * off:2 * off + n * 2].view(out_dtype).cpu(), v.to(out_dtype).reshape(-1))

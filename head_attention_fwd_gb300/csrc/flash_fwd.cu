@@ -52,6 +52,9 @@
 // Every wait is bounded: a pipeline stall records a code in the device
 // status word and the CTA winds down instead of hanging.
 
+#include <stdlib.h>
+#include <string.h>
+
 #include "common.h"
 #include "ptx.cuh"
 
@@ -946,6 +949,24 @@ FlashScratch flash_scratch_layout(int d, int grid) {
   return s;
 }
 
+// Whether cutting the last waves is expected to pay at d = 64.  Each extra
+// segment costs about 1.5 key-tile steps (Q load, pipeline restart, epilogue)
+// and a cut item's piece and merge about 3.5 more, so the cut must save at
+// least 8 steps per CTA, and items shorter than 16 key tiles never gain
+// (measured: B8 h12 S512 ran 14 % slower cut).  ATTN_SPLIT=force cuts
+// whenever the item count leaves a partial wave (used by the tests to cover
+// the cut path at small sizes); ATTN_SPLIT=never does not cut.
+static bool cut_pays(long long items, int n_kv, long long sms) {
+  const char* env = getenv("ATTN_SPLIT");
+  if (env && strcmp(env, "force") == 0) return true;
+  if (env && strcmp(env, "never") == 0) return false;
+  if (n_kv < 16) return false;
+  const long long grid = items * n_kv < sms ? items * n_kv : sms;
+  const long long steps_cut = (items * n_kv + grid - 1) / grid;
+  const long long steps_whole = (items + sms - 1) / sms * n_kv;
+  return steps_cut + 8 < steps_whole;
+}
+
 FlashPlan plan_flash(int B, int H, int S, int d, int num_sms, bool split) {
   FlashPlan pl;
   pl.n_qblk = (S + kItemRows - 1) / kItemRows;
@@ -959,7 +980,7 @@ FlashPlan plan_flash(int B, int H, int S, int d, int num_sms, bool split) {
     // persistent loop nest, and the last wave gains little from cutting)
     pl.mode = MODE_ONE;
     pl.grid = static_cast<int>(items);
-  } else if (!split || items % sms == 0) {
+  } else if (!split || items % sms == 0 || !cut_pays(items, pl.n_kv, sms)) {
     // whole items, round-robin over at most one CTA per SM
     pl.mode = MODE_PERSIST;
     pl.grid = static_cast<int>(items < sms ? items : sms);

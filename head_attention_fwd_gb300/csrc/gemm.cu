@@ -97,16 +97,22 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(bar(C::bar_accempty(a)), 8);  // one arrival per epilogue warp
     }
     mbar_init(bar(C::bar_drain()), 1);
-    *abort_flag = (*reinterpret_cast<volatile unsigned*>(p.status) != 0u) ? 1 : 0;
-    fence_mbar_init();
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
+  // Launched as a programmatic dependent: the set-up above overlaps the
+  // previous grid's tail, global memory is touched only after it completed.
+  griddep_wait();
+  if (threadIdx.x == 0) {
+    *abort_flag = (*reinterpret_cast<volatile unsigned*>(p.status) != 0u) ? 1 : 0;
+    fence_mbar_init();
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  griddep_launch_dependents();  // e.g. the attention kernel that reads this product
   const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_slot, 0);
   const WaitCtx wc{abort_flag, p.status, p.limit};
   const bool skip = *abort_flag != 0;
@@ -300,7 +306,18 @@ cudaError_t launch_impl(const GemmLaunch& a, cudaStream_t st) {
   p.status = a.status;
   p.limit = a.limit;
   const int grid = static_cast<int>(tiles < num_sms() ? tiles : num_sms());
-  kern<<<grid, 320, C::SMEM, st>>>(a.ta, a.tb, p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(320);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t le = cudaLaunchKernelEx(&cfg, kern, a.ta, a.tb, p);
+  if (le != cudaSuccess) return le;
   return cudaGetLastError();
 }
 

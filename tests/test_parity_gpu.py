@@ -24,6 +24,13 @@ def dev():
     return gpu_or_skip()
 
 
+@pytest.fixture
+def force_split(monkeypatch):
+    """Cut the last wave even where the library's cost rule would not (short
+    items), so that the cut-and-merge path is covered at small sizes."""
+    monkeypatch.setenv("ATTN_SPLIT", "force")
+
+
 def rand_qkv(B, h, S, d, dtype, layout, seed, qmul=1.0):
     g = torch.Generator().manual_seed(seed)
     shp = (B, h, S, d) if layout == 0 else (B, S, h, d)
@@ -41,9 +48,11 @@ SHAPES16 = [(1, 1, 1, 64), (1, 2, 128, 64), (2, 3, 300, 64), (1, 1, 513, 64), (1
 @pytest.mark.parametrize("layout", [0, 1])
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
 @pytest.mark.parametrize("split", [True, False], ids=["split", "whole"])
-def test_flash_matches_oracle(dev, shape, layout, dtype, split):
-    """split: items cut along the key axis over the SMs (at these sizes every
-    item is cut into pieces of one or a few key tiles); whole: attn_fwd."""
+def test_flash_matches_oracle(dev, shape, layout, dtype, split, monkeypatch):
+    """split: items cut along the key axis over the SMs (forced: at these sizes
+    every item is cut into pieces of one or a few key tiles); whole: attn_fwd."""
+    if split:
+        monkeypatch.setenv("ATTN_SPLIT", "force")
     B, h, S, d = shape
     q, k, v = rand_qkv(B, h, S, d, dtype, layout, seed=hash(shape) % 10000 + layout)
     o, lse = attn.attn_fwd(q.to(dev), k.to(dev), v.to(dev), layout=layout, want_lse=True, split=split)
@@ -60,7 +69,9 @@ PERSISTENT = [(1, 80, 512, 64), (2, 41, 300, 64), (1, 77, 640, 128), (1, 160, 25
 
 @pytest.mark.parametrize("shape", PERSISTENT, ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("split", [True, False], ids=["split", "whole"])
-def test_flash_persistent_schedule_matches_oracle(dev, shape, split):
+def test_flash_persistent_schedule_matches_oracle(dev, shape, split, monkeypatch):
+    if split:
+        monkeypatch.setenv("ATTN_SPLIT", "force")
     B, h, S, d = shape
     dtype = torch.bfloat16 if d == 128 else torch.float16
     q, k, v = rand_qkv(B, h, S, d, dtype, 0, seed=h * S + d)
@@ -75,7 +86,7 @@ def test_split_and_whole_agree(dev):
     """The cut-and-merge schedule and the whole-item schedule give the same
     result up to fp32 summation order (one 16-bit rounding step apart at most)."""
     q, k, v = (t.to(dev) for t in rand_qkv(1, 16, 4096, 64, torch.float16, 0, seed=7))
-    assert attn.attn_fwd_ws_bytes(1, 16, 4096, 64, torch.float16) > 0  # 256 items: not a multiple of the SMs
+    assert attn.attn_fwd_ws_bytes(1, 16, 4096, 64, torch.float16) > 0  # 256 items of 32 key tiles: cut by default
     o1, l1 = attn.attn_fwd(q, k, v, want_lse=True, split=True)
     o2, l2 = attn.attn_fwd(q, k, v, want_lse=True, split=False)
     device_status_ok()
@@ -84,7 +95,7 @@ def test_split_and_whole_agree(dev):
     assert (l1 - l2).abs().max().item() <= 1e-4
 
 
-def test_split_workspace_too_small_is_rejected(dev):
+def test_split_workspace_too_small_is_rejected(dev, force_split):
     import ctypes
     q, k, v = (t.to(dev) for t in rand_qkv(1, 16, 1024, 64, torch.float16, 0, seed=8))
     o = torch.empty_like(q)
@@ -101,7 +112,7 @@ def test_split_workspace_too_small_is_rejected(dev):
     device_status_ok()
 
 
-def test_split_schedule_replays_in_a_cuda_graph(dev):
+def test_split_schedule_replays_in_a_cuda_graph(dev, force_split):
     """A captured split launch replays with a fixed tag; its piece flags are
     cleared inside the graph, so every replay waits for its own pieces."""
     B, h, S, d = 1, 24, 700, 64
@@ -285,3 +296,11 @@ def test_mixed_fp32_inputs_match_oracle(dev, shape, layout, out_dtype):
     off = (n * 2 + 255) // 256 * 256
     assert torch.equal(ws[:n * 2].view(out_dtype).cpu(), q.to(out_dtype).reshape(-1))
     assert torch.equal(ws[2 * off:2 * off + n * 2].view(out_dtype).cpu(), v.to(out_dtype).reshape(-1))
+
+
+def test_cut_rule_keeps_short_items_whole(dev):
+    """Items of fewer than 16 key tiles are never cut by default (no scratch needed);
+    long items that leave a partial wave are."""
+    assert attn.attn_fwd_ws_bytes(8, 12, 512, 64, torch.float16) == 0
+    assert attn.attn_fwd_ws_bytes(2, 16, 8192, 64, torch.bfloat16) > 0
+    assert attn.attn_fwd_ws_bytes(1, 32, 16384, 128, torch.bfloat16) == 0   # d = 128: one item per CTA

@@ -304,3 +304,18 @@ def test_cut_rule_keeps_short_items_whole(dev):
     assert attn.attn_fwd_ws_bytes(8, 12, 512, 64, torch.float16) == 0
     assert attn.attn_fwd_ws_bytes(2, 16, 8192, 64, torch.bfloat16) > 0
     assert attn.attn_fwd_ws_bytes(1, 32, 16384, 128, torch.bfloat16) == 0   # d = 128: one item per CTA
+
+
+def test_grouped_layout_on_a_persistent_grid(dev):
+    """More (batch, head, 256-row) items than SMs in the head-group layout: CTAs take
+    several items in turn (d = 64) or one each (d = 128)."""
+    for d in (64, 128):
+        B, h, S, hg = 2, 40, 300, 4          # 2 * 40 * 2 = 160 items
+        g = torch.Generator().manual_seed(d)
+        dtype = torch.bfloat16
+        q, k, v = (torch.randn((B, h // hg, S, hg, d), generator=g).to(dtype) for _ in range(3))
+        o, lse = attn.attn_fwd_grouped(q.to(dev), k.to(dev), v.to(dev), want_lse=True)
+        device_status_ok()
+        o_ref, lse_ref = oracle.attention_grouped(q, k, v, hg, scale=1 / math.sqrt(d))
+        check_o(o, o_ref, dtype, f"grouped persistent d{d}")
+        check_lse(lse, lse_ref, f"grouped persistent d{d}")

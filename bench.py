@@ -61,6 +61,10 @@ def parse_args():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-extra", action="store_true", help="skip the comparison / other-workload lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--only", choices=["qkv", "naive", "mixed"],
+                    help="run only this path's calls (for profiling): the BERT-base projection + attention, "
+                         "the unfused two-pass path or the fp32-input path on the bench workload; prints its "
+                         "time per call, not the benchmark line")
     return ap.parse_args()
 
 
@@ -513,9 +517,60 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_only(args):
+    """`--steps` calls of one secondary path after `--warmup` untimed ones, for
+    ncu launch lists and captures of its kernels."""
+    import torch
+
+    import head_attention_fwd_gb300 as attn
+    from head_attention_fwd_gb300 import _build
+    from head_attention_fwd_gb300.inputs import WORKLOADS
+
+    _build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    if args.only == "qkv":
+        w = WORKLOADS["bert_base_qkv"]
+        g = torch.Generator(device=dev).manual_seed(w.seed)
+        x = torch.randn((w.B, w.S, w.D), generator=g, device=dev).to(w.torch_dtype)
+        wq = (torch.randn((w.D, 3 * w.D), generator=g, device=dev) * w.w_std).to(w.torch_dtype)
+        o = torch.empty((w.B, w.S, w.h, w.d), dtype=w.torch_dtype, device=dev)
+        ws = torch.empty(attn.qkv_proj_attn_workspace_bytes(w.B, w.S, w.D, x.dtype), dtype=torch.uint8, device=dev)
+        call = lambda i: attn.qkv_proj_attn(x, wq, w.h, o, ws, stream=stream)
+        flops = w.attn_flops + w.proj_flops
+    else:
+        w = WORKLOADS[WORKLOAD]
+        g = torch.Generator(device=dev).manual_seed(w.seed)
+        q, k, v = (torch.randn(w.shape(), generator=g, device=dev).to(w.torch_dtype) for _ in range(3))
+        o = torch.empty_like(q)
+        flops = w.attn_flops
+        if args.only == "naive":
+            ws = torch.empty(attn.attn_fwd_naive_workspace_bytes(w.B, w.h, w.S, q.dtype), dtype=torch.uint8,
+                             device=dev)
+            call = lambda i: attn.attn_fwd_naive(q, k, v, o, workspace=ws, layout=w.layout, stream=stream)
+        else:
+            q, k, v = (x.float() for x in (q, k, v))
+            ws = torch.empty(attn.attn_fwd_mixed_workspace_bytes(w.B, w.h, w.S, w.d, w.torch_dtype),
+                             dtype=torch.uint8, device=dev)
+            call = lambda i: attn.attn_fwd_mixed(q, k, v, o, workspace=ws, out_dtype=w.torch_dtype,
+                                                 layout=w.layout, stream=stream)
+    for i in range(args.warmup):
+        call(i)
+    torch.cuda.synchronize()
+    t = time_launches(call, args.steps, stream)
+    rc, detail = attn.attn_get_device_status()
+    if rc:
+        raise RuntimeError(f"device status: {attn.attn_status_string(rc)} ({detail:#x})")
+    print(json.dumps({"only": args.only, "calls": args.steps, "ms_per_call": t / args.steps * 1e3,
+                      "tflops": flops * args.steps / t / 1e12}), flush=True)
+
+
 def main():
     args = parse_args()
-    if args.impl == "reference":
+    if args.only:
+        run_only(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

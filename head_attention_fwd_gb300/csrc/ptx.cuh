@@ -64,9 +64,10 @@ __device__ __forceinline__ void raise_abort(const WaitCtx& w, uint32_t code) {
 }
 
 // With honor_abort = false the wait ignores the abort flag (used to drain
-// copies and MMAs already in flight before a CTA winds down).
-__device__ __forceinline__ bool mbar_wait_loop(uint32_t bar, uint32_t parity, const WaitCtx& w,
-                                               uint32_t code, bool honor_abort = true) {
+// copies and MMAs already in flight before a CTA winds down).  Out of line to
+// keep the polling loop out of hot code.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtx& w,
+                                                   uint32_t code, bool honor_abort = true) {
   const long long t0 = clock64();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -79,30 +80,19 @@ __device__ __forceinline__ bool mbar_wait_loop(uint32_t bar, uint32_t parity, co
     }
   }
 }
-// The same loop out of line, to keep it out of hot code (INL = false), or
-// inline where a kernel must call no functions (INL = true).
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtx& w,
-                                                   uint32_t code, bool honor_abort = true) {
-  return mbar_wait_loop(bar, parity, w, code, honor_abort);
-}
 
 // Bounded wait for the phase with the given parity to complete.
-template <bool INL = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtx& w,
                                           uint32_t code) {
   if (mbar_try_wait(bar, parity)) return true;
-  if constexpr (INL)
-    return mbar_wait_loop(bar, parity, w, code);
-  else
-    return mbar_wait_slow(bar, parity, w, code);
+  return mbar_wait_slow(bar, parity, w, code);
 }
 
 // Same, with the outcome made uniform over the calling warp (every lane must
 // call it): false on every lane if any lane gave up.
-template <bool INL = false>
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const WaitCtx& w,
                                                uint32_t code) {
-  const bool ok = mbar_wait<INL>(bar, parity, w, code);
+  const bool ok = mbar_wait(bar, parity, w, code);
   return __all_sync(0xffffffffu, ok);
 }
 

@@ -281,6 +281,28 @@ __global__ void __launch_bounds__(352, 1)
       mbar_init(bar(C::bar_ofree(t)), 128);
     }
     if constexpr (MODE != MODE_ONE) cta_work_init(p, work);
+    // Start pulling this CTA's first Q tiles and key/value tiles into L2 while
+    // the previous grid finishes: a prefetch delivers nothing to the SM, and
+    // L2 is where global memory is coherent, so it cannot see stale data.
+    Seg s0;
+    if (seg_at<MODE>(p, smem_u32(work), 0, s0)) {
+      const ItemPos ip = item_pos(p, s0.item);
+      auto pf = [&](const CUtensorMap* m, int e, int s) {
+        if constexpr (GROUPED)
+          tma_prefetch_4d(m, e, ip.hh % p.hg, s, ip.b * p.G + ip.hh / p.hg);
+        else if (p.hs_swap)
+          tma_prefetch_4d(m, e, ip.hh, s, ip.b);
+        else
+          tma_prefetch_4d(m, e, s, ip.hh, ip.b);
+      };
+      for (int c = 0; c < C::NCH; ++c) {
+        for (int tt = 0; tt < C::NQ; ++tt) pf(&tq, c * 64, ip.q0 + tt * C::BM);
+        for (int j = s0.jb; j < s0.je && j < s0.jb + C::STAGES; ++j) {
+          pf(&tk, c * 64, j * C::BN);
+          pf(&tv, c * 64, j * C::BN);
+        }
+      }
+    }
   }
   if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);

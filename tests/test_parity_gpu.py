@@ -319,3 +319,28 @@ def test_grouped_layout_on_a_persistent_grid(dev):
         o_ref, lse_ref = oracle.attention_grouped(q, k, v, hg, scale=1 / math.sqrt(d))
         check_o(o, o_ref, dtype, f"grouped persistent d{d}")
         check_lse(lse, lse_ref, f"grouped persistent d{d}")
+
+
+def test_split_launches_on_two_streams_do_not_interfere(dev, force_split):
+    """Cut launches running concurrently on two streams, each with its own
+    scratch: every result equals the same call made alone."""
+    shapes = [(1, 24, 700, 64), (2, 20, 900, 64)]
+    inputs, alone = [], []
+    for i, (B, h, S, d) in enumerate(shapes):
+        q, k, v = (t.to(dev) for t in rand_qkv(B, h, S, d, torch.float16, 0, seed=300 + i))
+        inputs.append((q, k, v))
+        alone.append(attn.attn_fwd(q, k, v, want_lse=True))
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in shapes]
+    outs = [[] for _ in shapes]
+    for rep in range(4):
+        for i, st in enumerate(streams):
+            st.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(st):
+                q, k, v = inputs[i]
+                outs[i].append(attn.attn_fwd(q, k, v, want_lse=True, stream=st))
+    torch.cuda.synchronize()
+    device_status_ok()
+    for i in range(len(shapes)):
+        for o, lse in outs[i]:
+            assert torch.equal(o, alone[i][0]) and torch.equal(lse, alone[i][1])

@@ -338,9 +338,12 @@ def run_e2e(attn, w, sets, stream, flops_step, steps, ws):
     import torch
 
     nb = 2
-    host_in = [tuple(t.cpu().pin_memory() for t in sets[i][:3]) for i in range(nb)]
-    host_out = [torch.empty_like(host_in[0][0]).pin_memory() for _ in range(nb)]
-    dev_sets = [tuple(torch.empty_like(t) for t in sets[0]) for _ in range(nb)]
+    # Q, K, V of a step side by side in one pinned buffer and one device
+    # buffer, so that a step is one 24 MiB upload rather than three
+    host_in = [torch.stack([t.cpu() for t in sets[i][:3]]).pin_memory() for i in range(nb)]
+    host_out = [torch.empty_like(sets[0][0], device="cpu").pin_memory() for _ in range(nb)]
+    dev_in = [torch.empty_like(host_in[0], device=sets[0][0].device) for _ in range(nb)]
+    dev_sets = [(dev_in[b][0], dev_in[b][1], dev_in[b][2], torch.empty_like(sets[0][0])) for b in range(nb)]
     up, down = torch.cuda.Stream(), torch.cuda.Stream()
     ev_up = [torch.cuda.Event() for _ in range(nb)]
     ev_comp = [torch.cuda.Event() for _ in range(nb)]
@@ -351,8 +354,7 @@ def run_e2e(attn, w, sets, stream, flops_step, steps, ws):
         qd, kd, vd, od = dev_sets[b]
         with torch.cuda.stream(up):
             up.wait_event(ev_comp[b])            # the kernel of step i-nb has read this set
-            for dst, src in zip((qd, kd, vd), host_in[b]):
-                dst.copy_(src, non_blocking=True)
+            dev_in[b].copy_(host_in[b], non_blocking=True)
             ev_up[b].record(up)
         stream.wait_event(ev_up[b])
         stream.wait_event(ev_down[b])            # O of step i-nb has been downloaded
@@ -382,9 +384,9 @@ def run_e2e(attn, w, sets, stream, flops_step, steps, ws):
     torch.cuda.synchronize()
     t = start.elapsed_time(end) / 1e3
     return {"value": flops_step * n / t / 1e12, "unit": UNIT,
-            "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in host_in[0]),
+            "h2d_bytes_per_step": host_in[0].numel() * host_in[0].element_size(),
             "d2h_bytes_per_step": host_out[0].numel() * host_out[0].element_size(),
-            "pipeline": "upload / compute / download streams over 2 device buffer sets",
+            "pipeline": "upload / compute / download streams over 2 device buffer sets, one upload per step",
             "ms_per_step": t / n * 1e3}
 
 

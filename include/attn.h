@@ -109,6 +109,12 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
  *   other arguments, lse and layouts as attn_fwd.  ATTN_F32 ignores the
  *   workspace (the fp32 path has no waves to balance).
  *
+ * Items are cut only where it pays: at d = 64, when they have at least 16
+ * key tiles and the cut saves at least 8 key-tile steps per SM (otherwise
+ * attn_fwd_ws runs as attn_fwd and attn_fwd_ws_bytes reports 0).  The
+ * environment variable ATTN_SPLIT=never disables the cut and ATTN_SPLIT=force
+ * cuts whenever the item count leaves a partial wave (for tests).
+ *
  * Errors: as attn_fwd, plus ATTN_E_WORKSPACE (misaligned, or smaller than
  * attn_fwd_ws_bytes for the current device) and ATTN_E_ALIAS (workspace
  * overlaps a tensor).
@@ -120,8 +126,9 @@ int attn_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse
 /*
  * Scratch bytes attn_fwd_ws needs on the current device (it depends on the
  * SM count): per SM 64 bytes of flags and 256 rows of (m, l) and d fp32
- * values.  0 when no item would be cut (the item count is a multiple of the
- * SM count), for ATTN_F32, for unsupported sizes, or without a device.
+ * values.  0 when no item would be cut (see above: d = 128, short items, an
+ * item count that fills whole waves), for ATTN_F32, for unsupported sizes, or
+ * without a device.
  */
 size_t attn_fwd_ws_bytes(int B, int h, int S, int d, int dtype);
 

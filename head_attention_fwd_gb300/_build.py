@@ -46,12 +46,21 @@ def _stamp() -> str:
     return h.hexdigest()
 
 
+def _code_only(text: str) -> str:
+    """The source without comments and with whitespace collapsed, so that a
+    comment edit does not change the hash of unchanged code."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def source_hash(files=("flash_fwd.cu", "ptx.cuh")) -> str:
-    """Short hash of the given kernel sources (used to tie profiles to code)."""
+    """Short hash of the given kernel sources' code (used to tie profiles to code)."""
     h = hashlib.sha256()
     for name in files:
-        with open(os.path.join(CSRC, name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(CSRC, name), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

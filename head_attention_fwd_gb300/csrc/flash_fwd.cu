@@ -7,19 +7,22 @@
 // ("WebGPU 算子优化：QKV 内存合并与 FlashAttention 分块计算",
 // §FlashAttention 分块计算原理与浏览器适配, gives the same merge rule).
 //
-// GB300 mapping (persistent: at most one CTA per SM, 11 warps, 192 KB of
-// shared memory):
+// GB300 mapping (at most one CTA per SM, 11 warps, 192 KB of shared memory):
 //   * work item = one (batch, head) and two 128-row Q tiles -- "ping-pong":
 //     while one tile's softmax runs on the CUDA cores, the tensor cores work
 //     on the other tile;
-//   * each CTA walks a list of segments: an item and a run of its key tiles.
-//     Whole items are dealt round-robin (item i on CTA i mod grid).  Given a
+//   * each CTA walks a list of segments: an item and a run of its key tiles
+//     (see Mode).  d = 128: one item per CTA.  d = 64: a persistent grid
+//     deals whole items round-robin (item i on CTA i mod grid); given a
 //     scratch buffer, the last one to two waves of items are instead cut
 //     into equal runs of key tiles, [g·U/grid, (g+1)·U/grid) for CTA g, so
 //     that every SM ends at the same time.  A cut item's later pieces leave
 //     their (m, l, unnormalised O) in the scratch; the CTA holding the piece
 //     that starts at key 0 merges them into its own with the same
 //     rescale-and-add rule that merges key tiles;
+//   * launched as a programmatic dependent: barrier set-up, tensor-memory
+//     allocation and an L2 prefetch of the first tiles overlap the previous
+//     grid; global memory is read only after griddepcontrol.wait;
 //   * warp 8: TMA producer.  Q tiles once per segment (at d = 64 into one of
 //     two buffers, so the next item's Q arrives during this one), then K and
 //     V tiles of 128 keys through a STAGES-deep ring of 128-byte-swizzled

@@ -545,20 +545,32 @@ __global__ void __launch_bounds__(352, 1)
     auto wait = [&](int i, uint32_t parity, uint32_t j) {
       return mbar_wait_warp(bar(i), parity, wc, code_of(ROLE_SOFTMAX, j));
     };
-    uint32_t r[4][32];  // this thread's row of S_t (kept intact for a possible second pass)
+    uint32_t r[4][32];  // this thread's row of S_t
+    // Ragged key tail: the columns from `valid` on do not exist.  They are set
+    // to -inf and the chunk maxima that the loads returned are taken again.
+    auto ragged_tail_max = [&](int valid, float (&mq)[4]) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          if (q * 32 + i >= valid) r[q][i] = f2u(-INFINITY);
+          mx = fmaxf(mx, u2f(r[q][i]));
+        }
+        mq[q] = mx;
+      }
+    };
     // p = 2^(s·c - m_ref) for the 128 keys, packed to 16-bit and stored to P_t
-    // chunk by chunk; returns the sum of p and, in mx, the raw row max.
-    auto exps_store = [&](float& mx) -> float {
+    // chunk by chunk; returns the sum of p.
+    auto exps_store = [&]() -> float {
       const uint64_t nm2 = pk64(-m_ref, -m_ref);
       uint64_t acc[4] = {0, 0, 0, 0};
-      float mxc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float s0 = u2f(r[q][2 * i]), s1 = u2f(r[q][2 * i + 1]);
-          mxc[i & 3] = max3(mxc[i & 3], s0, s1);
           float y0, y1;
           up64(ffma2(pk64(s0, s1), c2, nm2), y0, y1);
           const float e0 = ex2(y0), e1 = ex2(y1);
@@ -567,7 +579,6 @@ __global__ void __launch_bounds__(352, 1)
         }
         tmem_st16(tP + q * 16, pk);  // P columns [16q, 16q+16) hold keys [32q, 32q+32)
       }
-      mx = max3(mxc[0], mxc[1], fmaxf(mxc[2], mxc[3]));
       float a0, a1, a2, a3, a4, a5, a6, a7;
       up64(acc[0], a0, a1);
       up64(acc[1], a2, a3);
@@ -733,32 +744,16 @@ __global__ void __launch_bounds__(352, 1)
         const uint32_t n = n0 + static_cast<uint32_t>(j - jb);
         if (!(ok = wait(C::bar_sfull(t), n & 1, n))) break;
         tc_fence_after();
+        float mq[4];  // the loads' own row maxima, one per 32-column chunk
 #pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, r[q]);
+        for (int q = 0; q < 4; ++q) tmem_ld32_max(tS + q * 32, r[q], mq[q]);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_ld_wait(r[q]);
+        for (int q = 0; q < 4; ++q) tmem_ld_wait(r[q], mq[q]);
         tc_fence_before();
         mbar_arrive(bar(C::bar_sconsumed(t)));  // S_t may now be overwritten
         const int valid = p.S - j * C::BN;
-        if (valid < C::BN) {  // ragged key tail: these columns do not exist
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (q * 32 + i >= valid) r[q][i] = f2u(-INFINITY);
-        }
-        // four independent max chains (one per 32-column chunk) keep the
-        // register footprint small; the exponential pass dominates anyway
-        float mxc[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) mxc[k] = u2f(r[k][0]);
-#pragma unroll
-        for (int i = 1; i < 31; i += 2)
-#pragma unroll
-          for (int k = 0; k < 4; ++k) mxc[k] = max3(mxc[k], u2f(r[k][i]), u2f(r[k][i + 1]));
-        const float m_blk =
-            max3(max3(mxc[0], mxc[1], u2f(r[0][31])), max3(mxc[2], mxc[3], u2f(r[1][31])),
-                 max3(u2f(r[2][31]), u2f(r[3][31]), -INFINITY)) * c;
+        if (valid < C::BN) ragged_tail_max(valid, mq);
+        const float m_blk = max3(mq[0], mq[1], fmaxf(mq[2], mq[3])) * c;
         const bool move = m_blk > m_ref + kRescaleThreshold;  // always on a segment's first tile
         const bool any_move = __any_sync(0xffffffffu, move);
         float alpha = 1.f;
@@ -822,50 +817,38 @@ __global__ void __launch_bounds__(352, 1)
         const uint32_t n = n0 + static_cast<uint32_t>(j - jb);
         if (!(ok = wait(C::bar_sfull(t), n & 1, n))) break;
         tc_fence_after();
+        float mq[4];  // the loads' own row maxima, one per 32-column chunk
 #pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, r[q]);
+        for (int q = 0; q < 4; ++q) tmem_ld32_max(tS + q * 32, r[q], mq[q]);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_ld_wait(r[q]);
+        for (int q = 0; q < 4; ++q) tmem_ld_wait(r[q], mq[q]);
         const int valid = p.S - j * C::BN;
-        if (valid < C::BN) {  // ragged key tail: these columns do not exist
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (q * 32 + i >= valid) r[q][i] = f2u(-INFINITY);
-        }
+        if (valid < C::BN) ragged_tail_max(valid, mq);
+        const float m_blk = max3(mq[0], mq[1], fmaxf(mq[2], mq[3])) * c;
         if (j == jb) {  // empty history: the reference is this tile's max
-          float mxc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              mxc[i & 3] = max3(mxc[i & 3], u2f(r[q][2 * i]), u2f(r[q][2 * i + 1]));
-          m_ref = max3(mxc[0], mxc[1], fmaxf(mxc[2], mxc[3])) * c;
-        }
-        // One pass against the current reference, tracking the row max.
-        float mx;
-        float sum = exps_store(mx);
-        const float m_blk = mx * c;
-        const bool move = m_blk > m_ref + kRescaleThreshold;
-        if (__any_sync(0xffffffffu, move)) {  // rare: recompute P, rescale O (warp-uniform)
-          const float m_new = move ? m_blk : m_ref;
-          const float alpha = ex2(m_ref - m_new);
-          l *= alpha;
-          m_ref = m_new;
-          tmem_st_wait();
-          sum = exps_store(mx);
+          m_ref = m_blk;
+        } else {
+          // The tile max is known before any exponential: move the reference
+          // (rare) and rescale O first.  O_t already holds the previous
+          // P·V, which the issuer committed before this S_t.
+          const bool move = m_blk > m_ref + kRescaleThreshold;
+          if (__any_sync(0xffffffffu, move)) {  // warp-uniform
+            const float m_new = move ? m_blk : m_ref;
+            const float alpha = ex2(m_ref - m_new);
+            l *= alpha;
+            m_ref = m_new;
 #pragma unroll 1
-          for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t o[32];
-            tmem_ld32(tO + cc * 32, o);
-            tmem_ld_wait(o);
+            for (int cc = 0; cc < D / 32; ++cc) {
+              uint32_t o[32];
+              tmem_ld32(tO + cc * 32, o);
+              tmem_ld_wait(o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
-            tmem_st32(tO + cc * 32, o);
+              for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
+              tmem_st32(tO + cc * 32, o);
+            }
           }
         }
-        l += sum;
+        l += exps_store();
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar(C::bar_pready(t)));

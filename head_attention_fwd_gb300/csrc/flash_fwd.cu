@@ -34,15 +34,15 @@
 //     warp 9 issues both tiles in alternation;
 //   * warps 0-3 / 4-7: softmax of Q tile 0 / 1, one thread per query row
 //     (tensor-memory lane = row), so the row max and row sum are
-//     thread-local.  exp is 2^x on the SFU with scale·log2(e) folded into
-//     one packed FFMA; sums use packed fp32 adds and the max 3-input max.
-//     The running max only moves when the tile max exceeds it by more than
-//     2^8 (a factor of 256 in p, safe in fp16 and bf16); the result is exact
-//     either way because O and l always share the same reference.  So after
-//     the first tile the exponentials are computed against the current
-//     reference while the tile max is tracked in the same pass (S stays in
-//     registers and is released at once); only when some row's max moved by
-//     more than 2^8 does the warp recompute P and rescale O in tensor memory.
+//     thread-local.  S is read with tcgen05.ld.red (sm_103a), which hands
+//     back each 32-column chunk's maximum with the data, so the tile max
+//     costs three max operations instead of a pass over the row.  exp is
+//     2^x on the SFU with scale·log2(e) folded into one packed FFMA; sums use
+//     packed fp32 adds.  The running max only moves when the tile max exceeds
+//     it by more than 2^8 (a factor of 256 in p, safe in fp16 and bf16); the
+//     result is exact either way because O and l always share the same
+//     reference.  When some row's max does move (rare after the first tile),
+//     the warp rescales O in tensor memory before it writes P;
 //   * tensor memory, d = 64:  S0 | S1 | O0 | O1 | P0 | P1 (128+128+64+64+64+64)
 //     P has its own columns, so the next Q·K^T can be issued as soon as the
 //     softmax has read S, while it is still computing exponentials;

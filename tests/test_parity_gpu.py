@@ -147,20 +147,21 @@ def test_flash_explicit_scale_and_no_lse(dev, d):
     check_o(o, o_ref, torch.float16, "explicit scale")
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
-def test_flash_peaky_and_growing_scores(dev, dtype):
+def test_flash_peaky_and_growing_scores(dev, dtype, d):
     """Scores whose row maximum keeps growing from tile to tile (every key
     tile forces a rescale of the running output) plus isolated large keys."""
-    B, h, S, d = 1, 2, 1100, 64
+    B, h, S = 1, 2, 1100
     q, k, v = rand_qkv(B, h, S, d, torch.float32, 0, seed=5)
     ramp = torch.linspace(0.2, 3.0, S).view(1, 1, S, 1)
     k = k * ramp
     k[:, :, ::97] *= 6.0
-    q = q * 2.0
+    q = q * 2.0  # with scale 1/sqrt(d), the same spread of scaled scores at either head size
     q, k, v = q.to(dtype), k.to(dtype), v.to(dtype)
     o, lse = attn.attn_fwd(q.to(dev), k.to(dev), v.to(dev), want_lse=True)
     device_status_ok()
-    o_ref, lse_ref = oracle.attention(q, k, v, scale=1 / 8)
+    o_ref, lse_ref = oracle.attention(q, k, v, scale=1 / math.sqrt(d))
     check_o(o, o_ref, dtype, "peaky")
     check_lse(lse, lse_ref, "peaky")
 

@@ -90,6 +90,10 @@ def lib() -> ctypes.CDLL:
             L.attn_fwd_auto.restype = ci
             L.attn_compare.argtypes = [vp, vp, ctypes.c_longlong, ci, cf, ctypes.POINTER(cf), vp]
             L.attn_compare.restype = ci
+            L.attn_flash_schedule.argtypes = [ci, ci, ci, ci, ci, ci, ctypes.POINTER(ci), ctypes.POINTER(ci),
+                                              ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_longlong),
+                                              ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ci)]
+            L.attn_flash_schedule.restype = ci
             L.attn_abi_version.argtypes = []
             L.attn_abi_version.restype = ci
             _lib = L
@@ -140,6 +144,25 @@ def _check_dense(*ts):
 
 def _ptr(t):
     return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def attn_flash_schedule(B: int, h: int, S: int, d: int, num_sms: int, split: bool = True) -> dict:
+    """The attention kernel's work schedule for a problem on num_sms SMs (host
+    only, nothing is launched): mode, grid, dp_end, sk_units and, when items
+    are cut (mode 2), the run bounds `cut` and the merge ranges `g_last`."""
+    mode, grid = ctypes.c_int(), ctypes.c_int()
+    dp_end, sk_units = ctypes.c_longlong(), ctypes.c_longlong()
+    cut = (ctypes.c_longlong * 257)()
+    g_last = (ctypes.c_int * 256)()
+    rc = lib().attn_flash_schedule(B, h, S, d, num_sms, int(bool(split)), ctypes.byref(mode), ctypes.byref(grid),
+                                   ctypes.byref(dp_end), ctypes.byref(sk_units), cut, g_last)
+    if rc != 0:
+        raise ValueError(f"attn_flash_schedule: {attn_status_string(rc)}")
+    out = {"mode": mode.value, "grid": grid.value, "dp_end": dp_end.value, "sk_units": sk_units.value}
+    if sk_units.value > 0:
+        out["cut"] = list(cut[: grid.value + 1])
+        out["g_last"] = list(g_last[: grid.value])
+    return out
 
 
 def attn_fwd_ws_bytes(B: int, h: int, S: int, d: int, dtype) -> int:

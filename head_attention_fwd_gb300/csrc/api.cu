@@ -308,6 +308,21 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   return run_flash(q, k, v, o, lse, B, h, S, d, sc, layout, 1, dtype, rs, rs, ds, st);
 }
 
+int attn_flash_schedule(int B, int h, int S, int d, int num_sms, int split, int* mode, int* grid,
+                        long long* dp_end, long long* sk_units, long long* cut, int* g_last) {
+  if (B < 1 || h < 1 || S < 1 || num_sms < 1 || (d != 64 && d != 128)) return ATTN_E_SHAPE;
+  const attn::FlashPlan plan = attn::plan_flash(B, h, S, d, num_sms, split != 0);
+  if (mode) *mode = plan.mode;
+  if (grid) *grid = plan.grid;
+  if (dp_end) *dp_end = plan.dp_end;
+  if (sk_units) *sk_units = plan.sk_units;
+  if (plan.sk_units > 0) {
+    for (int g = 0; cut && g <= plan.grid; ++g) cut[g] = plan.cut[g];
+    for (int g = 0; g_last && g < plan.grid; ++g) g_last[g] = plan.g_last[g];
+  }
+  return 0;
+}
+
 size_t attn_fwd_ws_bytes(int B, int h, int S, int d, int dtype) {
   if (B < 1 || h < 1 || S < 1 || (dtype != ATTN_F16 && dtype != ATTN_BF16) || (d != 64 && d != 128))
     return 0;

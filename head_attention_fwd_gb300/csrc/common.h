@@ -31,16 +31,21 @@ struct FlashLaunch {
   bool clear_flags;             // zero the piece flags first (needed when the launch can be replayed)
 };
 
+// CTAs a cut plan may use: their run bounds travel in the kernel parameters.
+constexpr int kMaxCutGrid = 256;
+
 // Work list of the persistent attention kernel.  An item is one (batch, head)
 // and 256 query rows; items [0, dp_end) run whole, item i on CTA i % grid;
-// the sk_units key tiles of the remaining items are cut into equal runs, CTA
-// g taking units [g·sk_units/grid, (g+1)·sk_units/grid).
+// the sk_units key tiles of the remaining items are cut into equal
+// contiguous runs, CTA g taking units [cut[g], cut[g+1]).
 struct FlashPlan {
   int mode;                     // 0: one item per CTA; 1: persistent, whole items; 2: persistent + cut
   int grid;
   int n_qblk, n_kv;             // items per (batch, head); key tiles per item
   long long dp_end;
   long long sk_units;           // 0: no item is cut, no scratch is used
+  long long cut[kMaxCutGrid + 1];          // run bounds (mode 2)
+  unsigned short g_last[kMaxCutGrid];      // CTA holding the last key tile of the item CTA g's run ends in
 };
 // split = false: whole items only.  split = true: cut the last one to two
 // waves (only when the item count is not a multiple of num_sms).  The mode

@@ -135,7 +135,9 @@ struct Params {
   // work list (see FlashPlan)
   int grid;
   long long dp_end;          // items [0, dp_end) whole, round-robin
-  long long sk_units;        // key tiles of items [dp_end, ...), cut into equal runs
+  long long sk_units;        // key tiles of items [dp_end, ...), cut into runs
+  long long cut[kMaxCutGrid + 1];      // CTA g: cut units [cut[g], cut[g+1])
+  unsigned short g_last[kMaxCutGrid];  // see CtaWork
   // pieces of cut items: slot g belongs to CTA g (at most one piece per CTA)
   unsigned long long* flags;  // [grid][8]: tag once warp w's rows of slot g are written
   float2* ml;                 // [grid][256]: (m, l) of each row, m in log2 units
@@ -154,9 +156,9 @@ struct Seg {
   int jb, je, kind;
 };
 
-// The work list of one CTA, computed once by thread 0 into shared memory:
-// n_dp whole items (blockIdx.x + k·grid), then the key-tile run [u0, u1)
-// of the cut items, which starts inside item it0 = u0 / n_kv.
+// The work list of one CTA, set up once by thread 0 in shared memory: n_dp
+// whole items (blockIdx.x + k·grid), then the key-tile run [u0, u1) of the
+// cut items, which starts inside item it0 = u0 / n_kv.
 struct CtaWork {
   long long u0, u1, it0;
   int n_dp;
@@ -166,15 +168,18 @@ struct CtaWork {
 __device__ __forceinline__ void cta_work_init(const Params& p, CtaWork* cw) {
   const long long g = blockIdx.x;
   cw->n_dp = p.dp_end > g ? static_cast<int>((p.dp_end - g + p.grid - 1) / p.grid) : 0;
-  cw->u0 = g * p.sk_units / p.grid;
-  cw->u1 = (g + 1) * p.sk_units / p.grid;
+  if (p.sk_units > 0) {
+    cw->u0 = p.cut[g];
+    cw->u1 = p.cut[g + 1];
+    // A run that ends inside an item (a SEG_FIRST segment, or a piece that is
+    // not the item's last) leaves the rest to the CTAs up to g_last: the one
+    // whose run holds the item's last key tile.
+    cw->g_last = p.g_last[g];
+  } else {
+    cw->u0 = cw->u1 = 0;
+    cw->g_last = static_cast<int>(g);
+  }
   cw->it0 = cw->u0 / p.n_kv;
-  // A run that ends inside an item (a SEG_FIRST segment, or a piece that is
-  // not the item's last) leaves the rest to the CTAs up to g_last: the one
-  // whose run holds the item's last key tile.
-  const long long it_end = cw->u1 > cw->u0 ? (cw->u1 - 1) / p.n_kv : 0;
-  const long long last_unit = (it_end + 1) * p.n_kv - 1;
-  cw->g_last = p.sk_units > 0 ? static_cast<int>(((last_unit + 1) * p.grid - 1) / p.sk_units) : 0;
 }
 
 __device__ __forceinline__ long long lds_s64(uint32_t a) {
@@ -248,7 +253,7 @@ __device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
 template <int D, bool BF16, bool GROUPED, int MODE>
 __global__ void __launch_bounds__(352, 1)
     flash_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                     const __grid_constant__ CUtensorMap tv, const Params p) {
+                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ Params p) {
   using C = Cfg<D>;
   constexpr bool SPLIT = MODE == MODE_SPLIT;
   extern __shared__ uint8_t smem_raw[];
@@ -887,7 +892,7 @@ cudaError_t launch_impl(const FlashLaunch& a, const FlashPlan& plan, cudaStream_
   auto kern = flash_fwd_kernel<D, BF16, GROUPED, MODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  Params p;
+  Params p{};
   p.o = a.o;
   p.lse = a.lse;
   p.o_sb = a.o_sb;
@@ -907,6 +912,10 @@ cudaError_t launch_impl(const FlashLaunch& a, const FlashPlan& plan, cudaStream_
   p.grid = plan.grid;
   p.dp_end = plan.dp_end;
   p.sk_units = plan.sk_units;
+  if (plan.sk_units > 0) {
+    memcpy(p.cut, plan.cut, sizeof(long long) * (plan.grid + 1));
+    memcpy(p.g_last, plan.g_last, sizeof(unsigned short) * plan.grid);
+  }
   p.flags = nullptr;
   p.ml = nullptr;
   p.opart = nullptr;
@@ -975,8 +984,32 @@ static bool cut_pays(long long items, int n_kv, long long sms) {
   return steps_cut + 8 < steps_whole;
 }
 
+namespace {
+
+// Equal runs of the cut units, CTA g taking [g·U/grid, (g+1)·U/grid), and
+// for each CTA the CTA whose run holds the last key tile of the item its own
+// run ends in (the merge of a cut item waits for the CTAs up to that one).
+// Runs balanced by a per-segment cost estimate were tried: no gain on the
+// bench workload, and slower where an item is longer than a run, because a
+// key-0 part then waits for a long piece that ends with its own run.
+void equal_runs(FlashPlan& pl) {
+  const long long units = pl.sk_units;
+  for (int g = 0; g <= pl.grid; ++g) pl.cut[g] = g * units / pl.grid;
+  int h = 0;
+  for (int g = 0; g < pl.grid; ++g) {
+    pl.g_last[g] = static_cast<unsigned short>(g);
+    if (pl.cut[g + 1] <= pl.cut[g]) continue;
+    const long long last_unit = ((pl.cut[g + 1] - 1) / pl.n_kv + 1) * pl.n_kv - 1;
+    if (h < g) h = g;
+    while (pl.cut[h + 1] <= last_unit) ++h;
+    pl.g_last[g] = static_cast<unsigned short>(h);
+  }
+}
+
+}  // namespace
+
 FlashPlan plan_flash(int B, int H, int S, int d, int num_sms, bool split) {
-  FlashPlan pl;
+  FlashPlan pl{};
   pl.n_qblk = (S + kItemRows - 1) / kItemRows;
   pl.n_kv = (S + 127) / 128;
   const long long items = static_cast<long long>(B) * H * pl.n_qblk;
@@ -997,10 +1030,13 @@ FlashPlan plan_flash(int B, int H, int S, int d, int num_sms, bool split) {
     // equal runs of key tiles over every CTA
     pl.mode = MODE_SPLIT;
     const long long units_all = items * pl.n_kv;
-    pl.grid = static_cast<int>(units_all < sms ? units_all : sms);
+    long long grid = units_all < sms ? units_all : sms;
+    if (grid > kMaxCutGrid) grid = kMaxCutGrid;
+    pl.grid = static_cast<int>(grid);
     const long long waves = items / pl.grid;
     pl.dp_end = (waves > 0 ? waves - 1 : 0) * pl.grid;
     pl.sk_units = (items - pl.dp_end) * pl.n_kv;
+    equal_runs(pl);
   }
   return pl;
 }
@@ -1010,12 +1046,16 @@ cudaError_t launch_flash_fwd(const FlashLaunch& a, const FlashPlan& plan, cudaSt
   // The head-group layout has no scratch entry point: never cut.
   if (a.grouped && plan.mode == MODE_SPLIT) return cudaErrorInvalidValue;
   switch (plan.mode) {
-    case MODE_ONE:
-      if (a.grouped) return a.d == 64 ? launch_m<64, true, MODE_ONE>(a, plan, st) : launch_m<128, true, MODE_ONE>(a, plan, st);
-      return a.d == 64 ? launch_m<64, false, MODE_ONE>(a, plan, st) : launch_m<128, false, MODE_ONE>(a, plan, st);
+    case MODE_ONE:  // planned for d = 128 only
+      if (a.d != 128) return cudaErrorInvalidValue;
+      return a.grouped ? launch_m<128, true, MODE_ONE>(a, plan, st) : launch_m<128, false, MODE_ONE>(a, plan, st);
     case MODE_PERSIST:
+      // Whole items run on the cut-capable instance (with no cut units it
+      // deals items round-robin like MODE_PERSIST): its register allocation
+      // measured 0.7-1.5 % faster per key tile.  The head-group layout keeps
+      // the MODE_PERSIST instance.
       if (a.d != 64) return cudaErrorInvalidValue;
-      return a.grouped ? launch_m<64, true, MODE_PERSIST>(a, plan, st) : launch_m<64, false, MODE_PERSIST>(a, plan, st);
+      return a.grouped ? launch_m<64, true, MODE_PERSIST>(a, plan, st) : launch_m<64, false, MODE_SPLIT>(a, plan, st);
     case MODE_SPLIT:
       if (a.d != 64) return cudaErrorInvalidValue;
       return launch_m<64, false, MODE_SPLIT>(a, plan, st);

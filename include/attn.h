@@ -94,7 +94,8 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
  * attn_fwd deals whole items to at most one CTA per SM, so when the item
  * count is not a multiple of the SM count the last wave leaves SMs idle.
  * With the scratch, the last one to two waves of items are cut along the key
- * axis into equal runs of 128-key tiles, one run per SM.  Each later piece of
+ * axis into equal runs of 128-key tiles, one run per SM (see
+ * attn_flash_schedule).  Each later piece of
  * a cut item leaves its running max m, exp-sum l and unnormalised output in
  * the scratch; the piece that starts at key 0 merges them into its own with
  * the merge rule of "Transformer算子生态深度分析" §2.6 (each side rescaled by
@@ -122,6 +123,26 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
 int attn_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h,
                 int S, int d, float scale, int layout, int dtype, void* workspace, size_t ws_bytes,
                 void* stream);
+
+/*
+ * The work schedule attn_fwd_ws (split = 1) or attn_fwd (split = 0) would
+ * use for a 16-bit problem on a GPU with num_sms SMs.  Host only: no device is
+ * needed and nothing is launched.  Outputs (each may be NULL):
+ *   mode      0: one item per CTA (d = 128); 1: whole items on a persistent
+ *             grid, item i on CTA i mod grid; 2: as 1 for items [0, dp_end),
+ *             then the sk_units key tiles of the remaining items cut into
+ *             runs, CTA g taking tiles [cut[g], cut[g+1]) in item-major order
+ *   grid      CTAs launched
+ *   dp_end, sk_units   as above (sk_units = 0 unless mode = 2)
+ *   cut       [grid + 1] run bounds, written only in mode 2 (grid <= 256)
+ *   g_last    [grid], mode 2 only: the CTA whose run holds the last key tile
+ *             of the item in which CTA g's run ends
+ * An item is (batch, head, 256 query rows) with ceil(S / 128) key tiles.
+ * Honours ATTN_SPLIT like attn_fwd_ws.  Returns 0, or ATTN_E_SHAPE (B, h, S or
+ * num_sms < 1, d not 64 or 128).
+ */
+int attn_flash_schedule(int B, int h, int S, int d, int num_sms, int split, int* mode, int* grid,
+                        long long* dp_end, long long* sk_units, long long* cut, int* g_last);
 
 /*
  * Scratch bytes attn_fwd_ws needs on the current device (it depends on the

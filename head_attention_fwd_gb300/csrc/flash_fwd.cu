@@ -611,6 +611,14 @@ __global__ void __launch_bounds__(352, 1)
         if (!flag_wait_warp(p.flags + static_cast<long long>(g) * 8 + warp, p.tag, wc,
                             code_of(ROLE_EPILOGUE, static_cast<uint32_t>(g))))
           return false;
+      for (int g = static_cast<int>(blockIdx.x) + 1; g <= mg.g_last; ++g) {
+        // Pull the piece's row into L1 while the last P·V runs: the merge's
+        // loads below then hit L1 instead of waiting on L2 twice.  (The tag's
+        // acquire above orders them after the piece's stores.)
+        const float* src = p.opart + (static_cast<long long>(g) * kItemRows + rr) * D;
+#pragma unroll
+        for (int c = 0; c < D; c += 32) asm volatile("prefetch.global.L1 [%0];" ::"l"(src + c));
+      }
       for (int g = static_cast<int>(blockIdx.x) + 1; g <= mg.g_last; ++g)
         mg.m_new = fmaxf(mg.m_new, __ldcg(p.ml + static_cast<long long>(g) * kItemRows + rr).x);
       mg.a_own = ex2(m_ref - mg.m_new);
@@ -671,7 +679,7 @@ __global__ void __launch_bounds__(352, 1)
                   static_cast<long long>(in ? row : 0) * p.o_ss;
       if (SPLIT && sg.kind == SEG_FIRST) {
         // 32 columns per pass: own O from tensor memory, then every piece's
-        // 32 values with all 8 loads in flight at once.
+        // 32 values (from L1, see merge_stats) with all 8 loads in flight.
 #pragma unroll 1
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t o[32];
@@ -686,7 +694,7 @@ __global__ void __launch_bounds__(352, 1)
             const float4* src = reinterpret_cast<const float4*>(p.opart + slot * D) + cc * 8;
             float4 x[8];
 #pragma unroll
-            for (int v4 = 0; v4 < 8; ++v4) x[v4] = __ldcg(src + v4);
+            for (int v4 = 0; v4 < 8; ++v4) x[v4] = __ldca(src + v4);  // prefetched into L1
             const float wg = ex2(__ldcg(p.ml + slot).x - mg.m_new);
 #pragma unroll
             for (int v4 = 0; v4 < 8; ++v4) {

@@ -37,7 +37,10 @@ struct GCfg {
   // full[], empty[], acc_full[2], acc_empty[2], drain
   static constexpr int NBAR = 2 * STAGES + 5;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr uint32_t SMEM = OFF_MISC + 16 + 1024;
+  // epilogue staging: per epilogue warp 32 rows x 128 bytes
+  static constexpr uint32_t OFF_EPI = (OFF_MISC + 16 + 127) & ~127u;
+  static constexpr uint32_t EPI_WARP = 32 * 128;
+  static constexpr uint32_t SMEM = OFF_EPI + 8 * EPI_WARP + 1024;
   static constexpr uint32_t TMEM_COLS = 2 * BN;        // two accumulators
   __host__ __device__ static constexpr int bar_full(int s) { return s; }
   __host__ __device__ static constexpr int bar_empty(int s) { return STAGES + s; }
@@ -196,8 +199,37 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else {
     // -------------------------------------------------------- epilogue ----
+    // Each thread holds one output row of its warp's 32; the rows go out
+    // through a per-warp staging area so that every global store instruction
+    // writes whole 128-byte row segments (8 lanes per row, 4 rows) instead of
+    // 32 scattered 16-byte pieces.  16-byte unit u of staged row r sits at
+    // (u ^ (r & 7)) so that neither side has bank conflicts.
     const uint32_t wq = warp & 3u;               // tensor-memory lane quarter
-    const int half = (static_cast<int>(warp) - 2) >> 2;  // which half of the column chunks
+    const int half = (static_cast<int>(warp) - 2) >> 2;  // which half of the columns
+    uint8_t* stage = smem + C::OFF_EPI + (warp - 2u) * C::EPI_WARP;
+    const int esz = p.c_type == 0 ? 4 : 2;       // output element bytes
+    const long long ev = 16 / esz;               // elements per 16 bytes
+    const bool vec_ok = (reinterpret_cast<uintptr_t>(p.c) & 15u) == 0 && p.ldc % ev == 0 &&
+                        p.c_s1 % ev == 0 && p.c_s2 % ev == 0;
+    // Stages this thread's 8 16-byte units (one 128-byte row segment), then
+    // writes the warp's 32 segments to rows row0.. with coalesced stores.
+    auto flush = [&](const uint4 (&u16)[8], int row0, long long base, int col0) {
+      __syncwarp();  // the previous segment's reads are done
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        *reinterpret_cast<uint4*>(stage + lane * 128 + ((u ^ (lane & 7)) << 4)) = u16[u];
+      __syncwarp();
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int rr = it * 4 + static_cast<int>(lane >> 3), u = static_cast<int>(lane & 7);
+        const uint4 v = *reinterpret_cast<const uint4*>(stage + rr * 128 + ((u ^ (rr & 7)) << 4));
+        if (row0 + rr < p.M) {
+          uint8_t* dst = static_cast<uint8_t*>(p.c) +
+                         (base + static_cast<long long>(row0 + rr) * p.ldc + col0) * esz + u * 16;
+          *reinterpret_cast<uint4*>(dst) = v;
+        }
+      }
+    };
     int i = 0;
     for (int tile = blockIdx.x; tile < p.n_tiles; tile += gridDim.x, ++i) {
       const int a = i & 1;
@@ -206,47 +238,60 @@ __global__ void __launch_bounds__(320, 1)
       int z, mb, nb;
       tile_coords(tile, z, mb, nb);
       const int z1 = z % p.Z1, z2 = z / p.Z1;
-      const int row = mb * C::BM + static_cast<int>(wq * 32 + lane);
+      const int row0 = mb * C::BM + static_cast<int>(wq * 32);
+      const int row = row0 + static_cast<int>(lane);
       const bool in = row < p.M;
-      const long long off = z2 * p.c_s2 + z1 * p.c_s1 + static_cast<long long>(in ? row : 0) * p.ldc;
+      const long long base = z2 * p.c_s2 + z1 * p.c_s1;
+      const long long off = base + static_cast<long long>(in ? row : 0) * p.ldc;
       const uint32_t acc = tmem + ((wq * 32u) << 16) + a * BN;
+      // 128-byte row segments: 32 fp32 or 64 16-bit columns
+      const int seg_cols = p.c_type == 0 ? 32 : 64;
 #pragma unroll 1
-      for (int cc = half * (BN / 64); cc < (half + 1) * (BN / 64); ++cc) {
+      for (int c0 = half * (BN / 2); c0 < (half + 1) * (BN / 2); c0 += seg_cols) {
+        const int col0 = nb * BN + c0;
+        if (col0 >= p.N) break;
+        const bool fast = vec_ok && col0 + seg_cols <= p.N;
         uint32_t r[32];
-        tmem_ld32(acc + cc * 32, r);
+        tmem_ld32(acc + c0, r);
         tmem_ld_wait(r);
-        const int col0 = nb * BN + cc * 32;
-        if (!in || col0 >= p.N) continue;
-        const int nvalid = min(32, p.N - col0);
         if (p.c_type == 0) {
-          float* dst = static_cast<float*>(p.c) + off + col0;
-          const bool vec = nvalid == 32 && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0;
-          if (vec) {
+          if (fast) {
+            uint4 u16[8];
 #pragma unroll
-            for (int k = 0; k < 32; k += 4)
-              *reinterpret_cast<float4*>(dst + k) =
-                  make_float4(__uint_as_float(r[k]) * p.alpha, __uint_as_float(r[k + 1]) * p.alpha,
-                              __uint_as_float(r[k + 2]) * p.alpha, __uint_as_float(r[k + 3]) * p.alpha);
-          } else {
+            for (int u = 0; u < 8; ++u)
+              u16[u] = make_uint4(__float_as_uint(__uint_as_float(r[4 * u]) * p.alpha), __float_as_uint(__uint_as_float(r[4 * u + 1]) * p.alpha),
+                                  __float_as_uint(__uint_as_float(r[4 * u + 2]) * p.alpha), __float_as_uint(__uint_as_float(r[4 * u + 3]) * p.alpha));
+            flush(u16, row0, base, col0);
+          } else if (in) {
+            float* dst = static_cast<float*>(p.c) + off + col0;
+            const int nvalid = min(32, p.N - col0);
 #pragma unroll
             for (int k = 0; k < 32; ++k)
               if (k < nvalid) dst[k] = __uint_as_float(r[k]) * p.alpha;
           }
         } else {
-          uint16_t* dst = static_cast<uint16_t*>(p.c) + off + col0;
-          uint32_t pk[16];
+          uint32_t pk[32];
 #pragma unroll
           for (int k = 0; k < 16; ++k)
             pk[k] = pack2<BF16>(__uint_as_float(r[2 * k]) * p.alpha, __uint_as_float(r[2 * k + 1]) * p.alpha);
-          const bool vec = nvalid == 32 && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0;
-          if (vec) {
+          const bool second = col0 + 32 < p.N;  // columns [col0 + 32, col0 + 64) exist
+          if (second) {
+            tmem_ld32(acc + c0 + 32, r);
+            tmem_ld_wait(r);
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4)
-              reinterpret_cast<uint4*>(dst)[v4] =
-                  make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
-          } else {
+            for (int k = 0; k < 16; ++k)
+              pk[16 + k] = pack2<BF16>(__uint_as_float(r[2 * k]) * p.alpha, __uint_as_float(r[2 * k + 1]) * p.alpha);
+          }
+          if (fast) {
+            uint4 u16[8];
 #pragma unroll
-            for (int k = 0; k < 32; ++k)
+            for (int u = 0; u < 8; ++u) u16[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+            flush(u16, row0, base, col0);
+          } else if (in) {
+            uint16_t* dst = static_cast<uint16_t*>(p.c) + off + col0;
+            const int nvalid = min(64, p.N - col0);
+#pragma unroll
+            for (int k = 0; k < 64; ++k)
               if (k < nvalid) dst[k] = static_cast<uint16_t>(pk[k >> 1] >> ((k & 1) * 16));
           }
         }

@@ -14,7 +14,7 @@ def pytest_configure(config):
 
 def pytest_collection_modifyitems(config, items):
     # GPU tests are skipped, not failed, on a machine without a usable GPU only
-    # when explicitly deselected; with `-m gpu` on a GPU machine they must run.
+    # when explicitly deselected; with `-m gpu` on a machine with a GPU they must run.
     pass
 
 

@@ -145,6 +145,10 @@ struct Params {
   unsigned long long tag;     // unique per launch
 };
 
+// Kernel parameters (the three tensor maps and Params) must fit the 4 KB
+// parameter space of a launch.
+static_assert(3 * sizeof(CUtensorMap) + sizeof(Params) <= 4096, "kernel parameter space");
+
 // One segment of a CTA's work list.
 enum SegKind : int {
   SEG_WHOLE = 0,  // all key tiles of the item: normalise and store

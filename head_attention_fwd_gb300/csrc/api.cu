@@ -553,6 +553,7 @@ int qkv_proj_attn(const void* x, const void* w_qkv, void* o, int B, int S, int D
   g.c_s1 = g.c_s2 = 0;
   g.M = static_cast<int>(rows), g.N = 3 * D, g.K = D, g.Z1 = 1, g.Z2 = 1;
   g.bn = (3 * D) % 256 == 0 ? 256 : 128;
+  g.mb = g.bn == 256 ? 2 : 1;  // 256-row tiles: one third less operand traffic per flop
   g.b_kmajor = false;
   g.a_swap = g.b_swap = 0;
   g.bf16 = dtype == ATTN_BF16;

@@ -83,7 +83,8 @@ struct GemmLaunch {
   int c_type;                   // 0 = fp32, 1 = fp16, 2 = bf16
   long long ldc, c_s1, c_s2;
   int M, N, K, Z1, Z2;
-  int bn;                       // 64 or 128
+  int bn;                       // 64, 128 or 256: output columns per tile
+  int mb = 1;                   // 2: 256-row tiles (bn = 256, MN-major B only), 1: 128-row tiles
   bool b_kmajor;
   int a_swap, b_swap;           // 1: map dims are (inner, Z1, rows, Z2) instead of (inner, rows, Z1, Z2)
   bool bf16;                    // operand type

@@ -25,11 +25,14 @@
 namespace attn {
 namespace {
 
-template <int BN, bool BK>
+// MB = 2: a tile of 256 rows as two M = 128 products sharing each B stage
+// (one third less operand traffic per flop than two 128-row tiles).
+template <int BN, bool BK, int MB>
 struct GCfg {
-  static constexpr int BM = 128, BKE = 64;
-  static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 5 : 6);
-  static constexpr uint32_t A_BYTES = BM * 128;        // 128 rows x 64 elements x 2 B
+  static constexpr int BM = 128 * MB, BKE = 64;
+  static constexpr int STAGES = MB == 2 ? 3 : (BN == 256 ? 4 : (BN == 128 ? 5 : 6));
+  static constexpr uint32_t A_HALF = 128 * 128;        // 128 rows x 64 elements x 2 B
+  static constexpr uint32_t A_BYTES = MB * A_HALF;
   static constexpr uint32_t B_BYTES = BN * 128;        // BN x 64 x 2 B (either major)
   static constexpr uint32_t B_CHUNK = 64 * 128;        // MN-major: 64 k-rows x 64 n
   static constexpr uint32_t STAGE = A_BYTES + B_BYTES;
@@ -41,16 +44,20 @@ struct GCfg {
   static constexpr uint32_t OFF_EPI = (OFF_MISC + 16 + 127) & ~127u;
   static constexpr uint32_t EPI_WARP = 32 * 128;
   static constexpr uint32_t SMEM = OFF_EPI + 8 * EPI_WARP + 1024;
-  static constexpr uint32_t TMEM_COLS = 2 * BN;        // two accumulators
+  static constexpr int ACCS = MB * BN * 2 <= 512 ? 2 : 1;  // accumulator sets (tiles in flight)
+  static constexpr uint32_t ACC_COLS = MB * BN;
+  static constexpr uint32_t TMEM_COLS = ACCS * ACC_COLS;
   __host__ __device__ static constexpr int bar_full(int s) { return s; }
   __host__ __device__ static constexpr int bar_empty(int s) { return STAGES + s; }
   __host__ __device__ static constexpr int bar_accfull(int a) { return 2 * STAGES + a; }
   __host__ __device__ static constexpr int bar_accempty(int a) { return 2 * STAGES + 2 + a; }
   __host__ __device__ static constexpr int bar_drain() { return 2 * STAGES + 4; }
 };
-static_assert(GCfg<256, false>::SMEM <= 227 * 1024, "shared memory budget");
-static_assert(GCfg<128, false>::SMEM <= 227 * 1024, "shared memory budget");
-static_assert(GCfg<64, false>::SMEM <= 227 * 1024, "shared memory budget");
+static_assert(GCfg<256, false, 1>::SMEM <= 227 * 1024, "shared memory budget");
+static_assert(GCfg<256, false, 2>::SMEM <= 227 * 1024, "shared memory budget");
+static_assert(GCfg<128, false, 1>::SMEM <= 227 * 1024, "shared memory budget");
+static_assert(GCfg<64, false, 1>::SMEM <= 227 * 1024, "shared memory budget");
+static_assert(GCfg<256, false, 2>::TMEM_COLS == 512, "tensor memory budget");
 
 struct Params {
   void* c;
@@ -68,11 +75,11 @@ __device__ __forceinline__ uint32_t gcode(uint32_t role, int j) {
   return (KID_GEMM << 24) | (role << 16) | (static_cast<uint32_t>(j) & 0xffffu);
 }
 
-template <int BN, bool BKMAJOR, bool BF16>
+template <int BN, bool BKMAJOR, bool BF16, int MB>
 __global__ void __launch_bounds__(320, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
                 const Params p) {
-  using C = GCfg<BN, BKMAJOR>;
+  using C = GCfg<BN, BKMAJOR, MB>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sb = (raw + 1023u) & ~1023u;
@@ -146,7 +153,9 @@ __global__ void __launch_bounds__(320, 1)
         if (lane == 0) {
           const uint32_t st = sb + s * C::STAGE;
           mbar_expect_tx(bar(C::bar_full(s)), C::STAGE);
-          load(st, &ta, bar(C::bar_full(s)), kt * C::BKE, mb * C::BM, p.a_swap);
+#pragma unroll
+          for (int h = 0; h < MB; ++h)
+            load(st + h * C::A_HALF, &ta, bar(C::bar_full(s)), kt * C::BKE, mb * C::BM + h * 128, p.a_swap);
           if constexpr (BKMAJOR) {
             load(st + C::A_BYTES, &tb, bar(C::bar_full(s)), kt * C::BKE, nb * BN, p.b_swap);
           } else {
@@ -173,12 +182,12 @@ __global__ void __launch_bounds__(320, 1)
     int g = 0, i = 0;  // k-steps consumed, tiles done by this CTA
     bool ok = true;
     for (int tile = blockIdx.x; tile < p.n_tiles && ok; tile += gridDim.x, ++i) {
-      const int a = i & 1;
-      if (i >= 2 && !(ok = mbar_wait_warp(bar(C::bar_accempty(a)), ((i >> 1) - 1) & 1, wc,
-                                         gcode(ROLE_MMA, i))))
+      const int a = i % C::ACCS;
+      if (i >= C::ACCS && !(ok = mbar_wait_warp(bar(C::bar_accempty(a)), ((i / C::ACCS) - 1) & 1, wc,
+                                               gcode(ROLE_MMA, i))))
         break;
       tc_fence_after();
-      const uint32_t acc = tmem + a * BN;
+      const uint32_t acc = tmem + a * C::ACC_COLS;
       for (int kt = 0; kt < nk; ++kt, ++g) {
         const int s = g % C::STAGES, u = g / C::STAGES;
         if (!(ok = mbar_wait_warp(bar(C::bar_full(s)), u & 1, wc, gcode(ROLE_MMA, g)))) break;
@@ -187,7 +196,10 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int kk = 0; kk < C::BKE / 16; ++kk) {
           const uint32_t ka = (kk * 32) >> 4, kb = (BKMAJOR ? kk * 32 : kk * 2048) >> 4;
-          mma_ss_elect(acc, da + st16 + ka, db + st16 + kb, idesc, (kt > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int h = 0; h < MB; ++h)  // rows 128h.. of the tile into accumulator columns h·BN..
+            mma_ss_elect(acc + h * BN, da + st16 + ((h * C::A_HALF) >> 4) + ka, db + st16 + kb, idesc,
+                         (kt > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit_elect(bar(C::bar_empty(s)));
       }
@@ -205,7 +217,9 @@ __global__ void __launch_bounds__(320, 1)
     // 32 scattered 16-byte pieces.  16-byte unit u of staged row r sits at
     // (u ^ (r & 7)) so that neither side has bank conflicts.
     const uint32_t wq = warp & 3u;               // tensor-memory lane quarter
-    const int half = (static_cast<int>(warp) - 2) >> 2;  // which half of the columns
+    // The two warps of a lane quarter split the tile: by columns (MB = 1) or
+    // by its two 128-row halves (MB = 2).
+    const int half = (static_cast<int>(warp) - 2) >> 2;
     uint8_t* stage = smem + C::OFF_EPI + (warp - 2u) * C::EPI_WARP;
     const int esz = p.c_type == 0 ? 4 : 2;       // output element bytes
     const long long ev = 16 / esz;               // elements per 16 bytes
@@ -232,22 +246,23 @@ __global__ void __launch_bounds__(320, 1)
     };
     int i = 0;
     for (int tile = blockIdx.x; tile < p.n_tiles; tile += gridDim.x, ++i) {
-      const int a = i & 1;
-      if (!mbar_wait_warp(bar(C::bar_accfull(a)), (i >> 1) & 1, wc, gcode(ROLE_EPILOGUE, i))) break;
+      const int a = i % C::ACCS;
+      if (!mbar_wait_warp(bar(C::bar_accfull(a)), (i / C::ACCS) & 1, wc, gcode(ROLE_EPILOGUE, i))) break;
       tc_fence_after();
       int z, mb, nb;
       tile_coords(tile, z, mb, nb);
       const int z1 = z % p.Z1, z2 = z / p.Z1;
-      const int row0 = mb * C::BM + static_cast<int>(wq * 32);
+      const int row0 = mb * C::BM + (MB == 2 ? half * 128 : 0) + static_cast<int>(wq * 32);
       const int row = row0 + static_cast<int>(lane);
       const bool in = row < p.M;
       const long long base = z2 * p.c_s2 + z1 * p.c_s1;
       const long long off = base + static_cast<long long>(in ? row : 0) * p.ldc;
-      const uint32_t acc = tmem + ((wq * 32u) << 16) + a * BN;
+      const uint32_t acc = tmem + ((wq * 32u) << 16) + a * C::ACC_COLS + (MB == 2 ? half * BN : 0);
       // 128-byte row segments: 32 fp32 or 64 16-bit columns
       const int seg_cols = p.c_type == 0 ? 32 : 64;
 #pragma unroll 1
-      for (int c0 = half * (BN / 2); c0 < (half + 1) * (BN / 2); c0 += seg_cols) {
+      const int c_lo = MB == 2 ? 0 : half * (BN / 2), c_hi = MB == 2 ? BN : (half + 1) * (BN / 2);
+      for (int c0 = c_lo; c0 < c_hi; c0 += seg_cols) {
         const int col0 = nb * BN + c0;
         if (col0 >= p.N) break;
         const bool fast = vec_ok && col0 + seg_cols <= p.N;
@@ -324,10 +339,10 @@ int num_sms() {
   return n;
 }
 
-template <int BN, bool BKMAJOR, bool BF16>
+template <int BN, bool BKMAJOR, bool BF16, int MB = 1>
 cudaError_t launch_impl(const GemmLaunch& a, cudaStream_t st) {
-  using C = GCfg<BN, BKMAJOR>;
-  auto kern = gemm_kernel<BN, BKMAJOR, BF16>;
+  using C = GCfg<BN, BKMAJOR, MB>;
+  auto kern = gemm_kernel<BN, BKMAJOR, BF16, MB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   Params p;
@@ -371,6 +386,7 @@ cudaError_t dispatch(const GemmLaunch& a, cudaStream_t st) {
   if (a.bn == 64) return a.b_kmajor ? launch_impl<64, true, BF16>(a, st) : launch_impl<64, false, BF16>(a, st);
   if (a.bn == 128)
     return a.b_kmajor ? launch_impl<128, true, BF16>(a, st) : launch_impl<128, false, BF16>(a, st);
+  if (a.bn == 256 && a.mb == 2 && !a.b_kmajor) return launch_impl<256, false, BF16, 2>(a, st);
   if (a.bn == 256)
     return a.b_kmajor ? launch_impl<256, true, BF16>(a, st) : launch_impl<256, false, BF16>(a, st);
   return cudaErrorInvalidValue;

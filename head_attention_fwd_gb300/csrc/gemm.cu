@@ -260,8 +260,8 @@ __global__ void __launch_bounds__(320, 1)
       const uint32_t acc = tmem + ((wq * 32u) << 16) + a * C::ACC_COLS + (MB == 2 ? half * BN : 0);
       // 128-byte row segments: 32 fp32 or 64 16-bit columns
       const int seg_cols = p.c_type == 0 ? 32 : 64;
-#pragma unroll 1
       const int c_lo = MB == 2 ? 0 : half * (BN / 2), c_hi = MB == 2 ? BN : (half + 1) * (BN / 2);
+#pragma unroll 1
       for (int c0 = c_lo; c0 < c_hi; c0 += seg_cols) {
         const int col0 = nb * BN + c0;
         if (col0 >= p.N) break;

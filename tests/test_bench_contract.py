@@ -63,3 +63,16 @@ def test_bench_line_carries_roofline_clocks_and_e2e():
     assert d["e2e"]["h2d_bytes_per_step"] == 3 * 16 * 4096 * 64 * 2
     assert d["e2e"]["d2h_bytes_per_step"] == 16 * 4096 * 64 * 2
     assert "clocks" in d
+
+
+@pytest.mark.gpu
+def test_bench_value_stays_above_the_committed_floor():
+    """Performance regression check: the bench workload's throughput must stay
+    within about 10 % of the last committed measurement (tests/perf_floor.json)."""
+    from tests.gpu_common import gpu_or_skip
+    gpu_or_skip()
+    with open(os.path.join(ROOT, "tests", "perf_floor.json")) as f:
+        floor = json.load(f)
+    d = run_bench("--steps", "400", "--warmup", "5", "--no-extra", "--no-cpu")
+    assert d["config"]["workload"] == floor["workload"]
+    assert d["value"] >= floor["tflops_floor"], (d["value"], floor)

@@ -5,17 +5,22 @@
 // two products of the unfused comparison path (S = Q·K^T and O = P·V, same
 // chapter §2.2 and §2.4).
 //
-// Persistent: one CTA per SM walks the 128 x BN output tiles (tile index
+// Persistent: one CTA per SM walks the BM x BN output tiles (tile index
 // blockIdx.x, + gridDim.x, ...), 10 warps:
-//   warp 0     TMA producer: A (128 x 64, K-major) and B tiles through a
+//   warp 0     TMA producer: A (BM x 64, K-major) and B tiles through a
 //              STAGES-deep ring of 128-byte-swizzled shared-memory buffers,
 //              continuing across tiles;
-//   warp 1     tcgen05 issuer into one of two fp32 accumulators in tensor
-//              memory (128 lanes x BN columns each), alternating per tile;
-//   warps 2-9  epilogue: accumulator -> registers -> alpha, convert ->
-//              global (one thread per output row, two warps per tensor-memory
-//              lane quarter splitting the columns), while the issuer already
-//              fills the other accumulator with the next tile.
+//   warp 1     tcgen05 issuer into fp32 accumulators in tensor memory.  With
+//              BM = 128 there are two (128 lanes x BN columns each),
+//              alternating per tile.  With BM = 256 (the projection: two
+//              M = 128 products per k-step sharing each B stage, a third
+//              less operand traffic per flop) one accumulator of 512 columns;
+//   warps 2-9  epilogue: accumulator -> registers -> alpha, convert -> a
+//              per-warp shared-memory staging area -> global as whole
+//              128-byte row segments (one thread per output row; the two
+//              warps of a tensor-memory lane quarter split the columns, or
+//              with BM = 256 the two row halves), while the issuer already
+//              fills the other accumulator with the next tile (BM = 128).
 // B is either K-major ([N, K], e.g. K of S = Q·K^T) or MN-major ([K, N],
 // e.g. W_qkv or V) -- the tensor cores read both directly.
 

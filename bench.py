@@ -49,6 +49,7 @@ METRIC = "attention fwd TFLOP/s (4·B·h·S²·d) & % of GB300 FP16 tensor peak,
 UNIT = "TFLOP/s"
 WORKLOAD = "mha_f16_s4096"
 N_SETS = 8
+STEADY_S = 1.2  # seconds of the steady-state run added when the timed region is shorter
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 
 
@@ -61,10 +62,12 @@ def parse_args():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-extra", action="store_true", help="skip the comparison / other-workload lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    ap.add_argument("--only", choices=["qkv", "naive", "mixed"],
+    ap.add_argument("--only", choices=["qkv", "naive", "mixed", "fused"],
                     help="run only this path's calls (for profiling): the BERT-base projection + attention, "
-                         "the unfused two-pass path or the fp32-input path on the bench workload; prints its "
-                         "time per call, not the benchmark line")
+                         "the unfused two-pass path or the fp32-input path on the bench workload, or the fused "
+                         "attention (attn_fwd with its balancing scratch) on --workload; prints its time per "
+                         "call, not the benchmark line")
+    ap.add_argument("--shape", help="with --only fused: B,h,S overriding the workload's sizes (e.g. 1,2,16384)")
     return ap.parse_args()
 
 
@@ -153,6 +156,24 @@ class ClockSampler:
                 "power_w_max": max((float(r[3]) for r in rows if r[3].strip()[:1].isdigit()), default=None)}
 
 
+def clocks_once(gpu_index):
+    """One read-only nvidia-smi reading of the SM clock and throttle reasons."""
+    try:
+        r = subprocess.run(["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                            "-i", str(gpu_index)], capture_output=True, text=True, timeout=10)
+    except (OSError, subprocess.TimeoutExpired):
+        return None
+    row = [c.strip() for c in r.stdout.strip().split(",")]
+    if len(row) < 9:
+        return None
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    try:
+        return {"sm_mhz": float(row[1]), "sm_max_mhz": float(row[2]),
+                "reasons": [names[i] for i in range(4) if "Active" in row[5 + i] and "Not" not in row[5 + i]]}
+    except ValueError:
+        return None
+
+
 # ----------------------------------------------------------------- peaks ----
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -167,23 +188,20 @@ def measured_peaks():
 
 
 def profile_traffic(kernel_hash):
-    """DRAM bytes per launch of the attention kernel from the committed ncu
-    summary, if it was taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", f"flash_fwd_{WORKLOAD}.md")
-    vals = {}
+    """DRAM bytes per launch of the attention kernel, copied from the ncu
+    capture recorded in profiles/flash_fwd_<workload>.json, if that capture was
+    taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"flash_fwd_{WORKLOAD}.json")
     try:
         with open(path) as f:
-            for line in f:
-                if ":" in line and line.strip().startswith("- "):
-                    k, _, v = line.strip()[2:].partition(":")
-                    vals[k.strip()] = v.strip().strip("`")
-    except OSError:
+            rec = json.load(f)
+    except (OSError, ValueError):
         return None
-    if vals.get("kernel_source_hash") != kernel_hash:
+    if rec.get("kernel_source_hash") != kernel_hash:
         return None
     try:
-        return int(vals["dram_bytes_per_launch"])
-    except (KeyError, ValueError):
+        return int(rec["dram_bytes_per_launch"])
+    except (KeyError, TypeError, ValueError):
         return None
 
 
@@ -290,16 +308,42 @@ def run_ours(args):
         raise RuntimeError(f"device status after warm-up: {attn.attn_status_string(rc)} ({detail:#x})")
 
     sampler = ClockSampler(local) if rank == 0 else None
+    before = clocks_once(local) if rank == 0 else None
     barrier(world)
     torch.cuda.synchronize()
     t_local = time_launches(step, args.steps, stream)
     barrier(world)
     torch.cuda.synchronize()
+    after = clocks_once(local) if rank == 0 else None
     clocks = sampler.stop() if sampler else None
     t = max_over_ranks(t_local, world)
     rc, detail = attn.attn_get_device_status()
     if rc:
         raise RuntimeError(f"device status after timed region: {attn.attn_status_string(rc)}")
+
+    # A timed region shorter than about a second holds too few clock samples
+    # (the sampler reads every 100 ms): time the same call again over at least
+    # a second, with its own clock samples, as steady-state evidence.
+    steady = None
+    if t_local < STEADY_S:
+        n_st = int(math.ceil(STEADY_S / (t_local / args.steps)))
+        st_sampler = ClockSampler(local) if rank == 0 else None
+        t_st = time_launches(step, n_st, stream)
+        st_clocks = st_sampler.stop() if st_sampler else None
+        steady = {"value": aggregate_tflops(w.attn_flops, n_st, 1, t_st), "unit": UNIT, "steps": n_st,
+                  "ms_per_step": t_st / n_st * 1e3, "seconds": t_st, "clocks": st_clocks}
+    if rank == 0 and (clocks is None or not clocks.get("samples")):
+        src = steady["clocks"] if steady and steady["clocks"] else {}
+        reasons = sorted(set(src.get("reasons", [])) | set((before or {}).get("reasons", []))
+                         | set((after or {}).get("reasons", [])))
+        clocks = {"sm_mhz": src.get("sm_mhz", (after or before or {}).get("sm_mhz")),
+                  "sm_max_mhz": src.get("sm_max_mhz", (after or before or {}).get("sm_max_mhz")),
+                  "reasons": reasons, "samples": 0, "before": before, "after": after,
+                  "note": (f"the {t_local * 1e3:.1f} ms timed region held no 100 ms sample; sm_mhz and reasons "
+                           "come from the steady-state run of the same call and from one reading "
+                           "right before and after the timed region")}
+    elif clocks is not None:
+        clocks["before"], clocks["after"] = before, after
 
     flops_step = w.attn_flops
     value = aggregate_tflops(flops_step, args.steps, world, t)
@@ -350,6 +394,8 @@ def run_ours(args):
         from head_attention_fwd_gb300.inputs import make_qkv as mk
         qc, kc, vc = mk(w)
         line["cpu_baseline"] = cpu_baseline(w, qc, kc, vc)
+    if steady:
+        extra["steady_state"] = steady
     if extra:
         line["extra"] = extra
     print(json.dumps(line), flush=True)
@@ -577,6 +623,18 @@ def run_only(args):
         ws = torch.empty(attn.qkv_proj_attn_workspace_bytes(w.B, w.S, w.D, x.dtype), dtype=torch.uint8, device=dev)
         call = lambda i: attn.qkv_proj_attn(x, wq, w.h, o, ws, stream=stream)
         flops = w.attn_flops + w.proj_flops
+    elif args.only == "fused":
+        from head_attention_fwd_gb300.inputs import make_qkv
+        w = WORKLOADS[args.workload]
+        if args.shape:
+            B, h, S = (int(x) for x in args.shape.split(","))
+            w = w.with_(B=B, h=h, S=S)
+        q, k, v = (t.to(dev) for t in make_qkv(w))
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.h, w.S), dtype=torch.float32, device=dev) if w.want_lse else None
+        ws = split_scratch(attn, w, dev) if w.dtype != "f32" else None
+        call = lambda i: attn.attn_fwd(q, k, v, o, lse, layout=w.layout, stream=stream, workspace=ws)
+        flops = w.attn_flops
     else:
         w = WORKLOADS[WORKLOAD]
         g = torch.Generator(device=dev).manual_seed(w.seed)
@@ -600,7 +658,8 @@ def run_only(args):
     rc, detail = attn.attn_get_device_status()
     if rc:
         raise RuntimeError(f"device status: {attn.attn_status_string(rc)} ({detail:#x})")
-    print(json.dumps({"only": args.only, "calls": args.steps, "ms_per_call": t / args.steps * 1e3,
+    print(json.dumps({"only": args.only, "workload": w.name, "B": w.B, "h": w.h, "S": w.S, "d": w.d,
+                      "calls": args.steps, "ms_per_call": t / args.steps * 1e3,
                       "tflops": flops * args.steps / t / 1e12}), flush=True)
 
 

@@ -315,14 +315,18 @@ def qkv_proj_attn_noalloc(x, w_qkv, h: int, o=None, *, stream=None):
     device memory: the projection goes to the library's fixed static scratch
     (ATTN_NOALLOC_SCRATCH_BYTES = 32 MiB per device).  The C call allocates nothing;
     only the optional output below is allocated here, when ``o`` is not given.
-    Returns o [B,S,h,d]."""
+    The scratch belongs to the current device, so the call runs with x's device
+    made current.  Returns o [B,S,h,d]."""
     torch = _torch()
     B, S, D = (int(n) for n in x.shape)
     if o is None:
         o = torch.empty((B, S, h, D // h), dtype=x.dtype, device=x.device)
     _check_dense(x, w_qkv, o)
-    rc = lib().qkv_proj_attn_noalloc(_ptr(x), _ptr(w_qkv), _ptr(o), B, S, D, h, dtype_code(x.dtype),
-                                     _stream_ptr(stream))
+    if w_qkv.device != x.device or o.device != x.device:
+        raise ValueError("x, w_qkv and o must be on one device")
+    with torch.cuda.device(x.device):
+        rc = lib().qkv_proj_attn_noalloc(_ptr(x), _ptr(w_qkv), _ptr(o), B, S, D, h, dtype_code(x.dtype),
+                                         _stream_ptr(stream))
     if rc:
         raise AttnError(rc, "qkv_proj_attn_noalloc")
     return o

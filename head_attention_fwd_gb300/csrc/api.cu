@@ -519,27 +519,45 @@ size_t qkv_proj_attn_workspace_bytes(int B, int S, int D, int dtype) {
   return round256(static_cast<size_t>(B) * S * 3 * D * 2);
 }
 
-int qkv_proj_attn(const void* x, const void* w_qkv, void* o, int B, int S, int D, int h, int dtype,
-                  void* workspace, size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace attn {
+
+int validate_qkv_proj(const void* x, const void* w_qkv, const void* o, int B, int S, int D, int h,
+                      int dtype) {
   if (!x || !w_qkv || !o) return ATTN_E_NULL;
   if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_E_DTYPE;
   if (B < 1 || S < 1 || h < 1 || D < 1 || D % h) return ATTN_E_SHAPE;
   const int d = D / h;
   if (d != 64 && d != 128) return ATTN_E_SHAPE;
   const long long rows = static_cast<long long>(B) * S;
-  if (rows * 3 * D > (1LL << 40) || static_cast<long long>(B) * h * ((S + 255) / 256) > 0x7fffffffLL ||
+  if (rows > 0x7fffffffLL || rows * 3 * D > (1LL << 40) ||
+      static_cast<long long>(B) * h * ((S + 255) / 256) > 0x7fffffffLL ||
       ((rows + 127) / 128) * ((3LL * D + 127) / 128) > 0x7fffffffLL)
     return ATTN_E_SHAPE;
   if (!aligned(x, 16) || !aligned(w_qkv, 16) || !aligned(o, 16)) return ATTN_E_ALIGN;
+  const size_t xb = static_cast<size_t>(rows) * D * 2, wb = static_cast<size_t>(D) * 3 * D * 2;
+  if (overlap(o, xb, x, xb) || overlap(o, xb, w_qkv, wb)) return ATTN_E_ALIAS;
+  return ATTN_OK;
+}
+
+}  // namespace attn
+
+extern "C" {
+
+int qkv_proj_attn(const void* x, const void* w_qkv, void* o, int B, int S, int D, int h, int dtype,
+                  void* workspace, size_t ws_bytes, void* stream) {
+  int rc = attn::validate_qkv_proj(x, w_qkv, o, B, S, D, h, dtype);
+  if (rc) return rc;
+  const int d = D / h;
+  const long long rows = static_cast<long long>(B) * S;
   const size_t need = qkv_proj_attn_workspace_bytes(B, S, D, dtype);
   if (!workspace || ws_bytes < need || !aligned(workspace, 256)) return ATTN_E_WORKSPACE;
   const size_t xb = static_cast<size_t>(rows) * D * 2, wb = static_cast<size_t>(D) * 3 * D * 2;
-  if (overlap(o, xb, x, xb) || overlap(o, xb, w_qkv, wb) || overlap(o, xb, workspace, need) ||
-      overlap(workspace, need, x, xb) || overlap(workspace, need, w_qkv, wb))
+  if (overlap(o, xb, workspace, need) || overlap(workspace, need, x, xb) || overlap(workspace, need, w_qkv, wb))
     return ATTN_E_ALIAS;
   DeviceState* ds = nullptr;
-  int rc = device_setup(&ds);
-  if (rc) return rc;
+  if ((rc = device_setup(&ds))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   // 1. QKV = X · W_qkv  -> workspace [B·S, 3D]
@@ -560,7 +578,6 @@ int qkv_proj_attn(const void* x, const void* w_qkv, void* o, int B, int S, int D
   g.alpha = 1.f;
   g.status = ds->status;
   g.limit = wait_limit();
-  if (rows > 0x7fffffffLL) return ATTN_E_SHAPE;
   if ((rc = to_rc(attn::launch_gemm(g, st)))) return rc;
 
   // 2. attention on the projection in place: Q, K, V are the three column

@@ -123,8 +123,14 @@ struct NaiveSoftmaxLaunch {
 cudaError_t launch_naive_softmax(const NaiveSoftmaxLaunch& a, cudaStream_t st);
 
 // max |a - b| over n elements of two device buffers (dtype as attn.h);
-// synchronises the stream and writes the result to *host_max.  Uses one
-// statically declared device word: concurrent calls on different streams race.
+// synchronises the stream and writes the result to *host_max.  Each call
+// accumulates into its own one of 64 statically declared device words, taken
+// in turn, so calls in flight at the same time do not share a result.
+// Argument checks of the fused QKV projection + attention entry points
+// (pointers, dtype, shape, 16-byte alignment, output overlapping an input);
+// ATTN_OK or a negative ATTN_E_* code.  Makes no CUDA call.
+int validate_qkv_proj(const void* x, const void* w_qkv, const void* o, int B, int S, int D, int h, int dtype);
+
 cudaError_t launch_max_abs_diff(const void* a, const void* b, long long n, int dtype,
                                 float* host_max, cudaStream_t st);
 

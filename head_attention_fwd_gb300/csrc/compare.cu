@@ -5,6 +5,8 @@
 
 #include <string.h>
 
+#include <atomic>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -13,9 +15,14 @@
 namespace attn {
 namespace {
 
-// Bits of the running maximum (non-negative floats order like their bits;
-// a NaN difference is recorded as +inf).
-__device__ unsigned g_max_bits;
+// Result words: each call takes the next one in turn, so that up to
+// kSlots calls in flight at once (on different streams or host threads)
+// accumulate into different words.  A word holds the bits of the running
+// maximum (non-negative floats order like their bits; a NaN difference is
+// recorded as +inf).
+constexpr unsigned kSlots = 64;
+__device__ unsigned g_max_bits[kSlots];
+std::atomic<unsigned> g_next_slot{0};
 
 __device__ __forceinline__ float load_as_float(const void* p, long long i, int dtype) {
   if (dtype == 1) return __half2float(static_cast<const __half*>(p)[i]);
@@ -23,10 +30,10 @@ __device__ __forceinline__ float load_as_float(const void* p, long long i, int d
   return static_cast<const float*>(p)[i];
 }
 
-__global__ void clear_kernel() { g_max_bits = 0u; }
+__global__ void clear_kernel(unsigned slot) { g_max_bits[slot] = 0u; }
 
 __global__ void __launch_bounds__(256) max_abs_diff_kernel(const void* a, const void* b, long long n,
-                                                           int dtype) {
+                                                           int dtype, unsigned slot) {
   float m = 0.f;
   for (long long i = blockIdx.x * 256LL + threadIdx.x; i < n; i += 256LL * gridDim.x) {
     const float d = fabsf(load_as_float(a, i, dtype) - load_as_float(b, i, dtype));
@@ -34,20 +41,23 @@ __global__ void __launch_bounds__(256) max_abs_diff_kernel(const void* a, const 
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if ((threadIdx.x & 31) == 0) atomicMax(&g_max_bits, __float_as_uint(m));
+  if ((threadIdx.x & 31) == 0) atomicMax(&g_max_bits[slot], __float_as_uint(m));
 }
 
 }  // namespace
 
 cudaError_t launch_max_abs_diff(const void* a, const void* b, long long n, int dtype, float* host_max,
                                 cudaStream_t st) {
-  clear_kernel<<<1, 1, 0, st>>>();
+  const unsigned slot = g_next_slot.fetch_add(1u) % kSlots;
+  clear_kernel<<<1, 1, 0, st>>>(slot);
   const long long blocks = (n + 255) / 256;
-  max_abs_diff_kernel<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0, st>>>(a, b, n, dtype);
+  max_abs_diff_kernel<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0, st>>>(a, b, n, dtype,
+                                                                                             slot);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   unsigned bits = 0;
-  if ((e = cudaMemcpyFromSymbolAsync(&bits, g_max_bits, sizeof bits, 0, cudaMemcpyDeviceToHost, st)) !=
+  if ((e = cudaMemcpyFromSymbolAsync(&bits, g_max_bits, sizeof bits, slot * sizeof(unsigned),
+                                     cudaMemcpyDeviceToHost, st)) !=
       cudaSuccess)
     return e;
   if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return e;

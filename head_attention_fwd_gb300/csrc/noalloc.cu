@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "attn.h"
+#include "common.h"
 
 namespace {
 
@@ -45,9 +46,11 @@ int scratch_on_current_device(void** out) {
 
 extern "C" int qkv_proj_attn_noalloc(const void* x, const void* w_qkv, void* o, int B, int S, int D,
                                      int h, int dtype, void* stream) {
+  // The same checks as qkv_proj_attn first, so that a bad argument is named
+  // as such even on a problem too large for the scratch.
+  const int rc0 = attn::validate_qkv_proj(x, w_qkv, o, B, S, D, h, dtype);
+  if (rc0) return rc0;
   const size_t need = qkv_proj_attn_workspace_bytes(B, S, D, dtype);
-  if (need == 0)  // invalid sizes or dtype: let the regular entry point name the error
-    return qkv_proj_attn(x, w_qkv, o, B, S, D, h, dtype, nullptr, 0, stream);
   if (need > ATTN_NOALLOC_SCRATCH_BYTES) return ATTN_E_SCRATCH_LIMIT;
   void* ws = nullptr;
   const int rc = scratch_on_current_device(&ws);

@@ -38,7 +38,12 @@
  *    reported by the runtime while enqueuing.
  *  - Device-side faults of the pipeline (a wait that exceeded its time
  *    limit) do not trap: the kernel records a code in the device status
- *    word and returns; read it with attn_get_device_status.
+ *    word and returns; read it with attn_get_device_status.  There is one
+ *    status word per device, shared by every stream: once a timeout is
+ *    recorded, every attention kernel launched afterwards on that device, on
+ *    any stream, does no work (its output is left undefined) until
+ *    attn_get_device_status has read and cleared the word.  Callers that use
+ *    several streams should check the status after each batch of work.
  */
 #ifndef ATTN_GB300_H
 #define ATTN_GB300_H
@@ -256,7 +261,8 @@ size_t qkv_proj_attn_workspace_bytes(int B, int S, int D, int dtype);
  * [B, S, 3D] projection goes to a fixed scratch array of
  * ATTN_NOALLOC_SCRATCH_BYTES that the library declares statically in device
  * memory (every GPU that loads the library holds it until the process exits).
- * The call itself allocates nothing.
+ * The call itself calls no allocator (see below for what the first call on a
+ * device implies).
  *
  *   x, w_qkv, o, B, S, D, h, dtype, stream   as for qkv_proj_attn.
  *
@@ -264,13 +270,20 @@ size_t qkv_proj_attn_workspace_bytes(int B, int S, int D, int dtype);
  * ATTN_NOALLOC_SCRATCH_BYTES (32 MiB, e.g. B·S <= 7281 at D = 768 in fp16);
  * larger problems return ATTN_E_SCRATCH_LIMIT and launch nothing.
  * The first call on each device resolves the scratch array's device address
- * (with that device current), so make that first call before any stream
- * capture.  All calls share the one array and it keeps the last call's
+ * (with that device current).  Under CUDA's default lazy module loading, that
+ * first call is also what loads the part of the library holding the array:
+ * the driver then reserves its 32 MiB of device memory, which can fail with
+ * cudaErrorMemoryAllocation (returned as a positive code) and may synchronise
+ * the device.  So make the first call on each device during set-up, before any
+ * stream capture and while memory is still free, or run the process with
+ * CUDA_MODULE_LOADING=EAGER so that the array is reserved when the context is
+ * created.  Every later call allocates nothing and does not synchronise.
+ * All calls share the one array and it keeps the last call's
  * contents; nothing in it needs to start at zero because the projection
  * overwrites every element it later reads.  Calls that overlap on the GPU
  * (for example on two streams at once) race on the array: serialise them.
- * Errors: as qkv_proj_attn (without the workspace checks), plus
- * ATTN_E_SCRATCH_LIMIT.
+ * Errors: as qkv_proj_attn (without the workspace checks, and checked first),
+ * plus ATTN_E_SCRATCH_LIMIT.
  */
 #define ATTN_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 int qkv_proj_attn_noalloc(const void* x, const void* w_qkv, void* o, int B, int S, int D, int h,
@@ -304,6 +317,9 @@ int attn_fwd_auto(const void* q, const void* k, const void* v, void* o, float* l
  * (host, may be NULL).  Returns ATTN_OK when it is <= atol, ATTN_E_MISMATCH
  * otherwise (a NaN counts as a mismatch), or an error.  The page uses
  * atol = 1e-3; for 16-bit outputs the two kernels also round P differently.
+ * Each call accumulates into its own device result word (64 statically
+ * declared words, taken in turn), so up to 64 calls may run at the same time
+ * on different streams or host threads without sharing a result.
  */
 int attn_compare(const void* a, const void* b, long long n, int dtype, float atol, float* max_abs,
                  void* stream);

@@ -182,6 +182,27 @@ def test_qkv_proj_attn_validation_and_workspace(L):
     assert proj(ws=K) == E["ALIAS"]
 
 
+def test_qkv_proj_attn_noalloc_checks_arguments_before_the_scratch_limit(L):
+    """A bad argument is reported as such even on a problem too large for the
+    fixed scratch; only a valid problem that is too large gets the limit code."""
+    vp = ctypes.c_void_p
+    SCRATCH_LIMIT = -10
+
+    def noalloc(x=Q, w=K, o=O, B=8, S=1024, D=768, h=12, dtype=1):
+        return L.qkv_proj_attn_noalloc(vp(x), vp(w), vp(o), B, S, D, h, dtype, vp(0))
+
+    assert 8 * 1024 * 3 * 768 * 2 > 32 << 20              # the default problem is over the limit
+    assert noalloc() == SCRATCH_LIMIT
+    assert noalloc(h=8) == E["SHAPE"]                      # d = 96
+    assert noalloc(D=770) == E["SHAPE"]                    # D % h != 0
+    assert noalloc(x=None) == E["NULL"]
+    assert noalloc(dtype=0) == E["DTYPE"]
+    assert noalloc(w=K + 4) == E["ALIGN"]
+    assert noalloc(o=Q + 1024) == E["ALIAS"]
+    if not torch.cuda.is_available():
+        assert noalloc(B=1, S=64) == E["DEVICE"]           # valid and within the limit
+
+
 def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(attn, "_lib", None)
     monkeypatch.setattr(attn, "LIB_PATH", str(tmp_path / "missing.so"))

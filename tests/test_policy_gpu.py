@@ -1,11 +1,15 @@
-"""attn_fwd_auto runs the kernel the policy picks, and the numeric-agreement
-guard passes on the two kernels' outputs and catches a planted difference."""
+"""attn_fwd_auto runs the kernel the policy picks, its output matches the fp64
+oracle, and the numeric-agreement guard passes on the two kernels' outputs and
+catches a planted difference."""
+
+import math
 
 import pytest
 import torch
 
 import head_attention_fwd_gb300 as attn
-from tests.gpu_common import TOL16_MAX, device_status_ok, gpu_or_skip
+import oracle
+from tests.gpu_common import TOL16_MAX, check_o, device_status_ok, gpu_or_skip
 
 pytestmark = pytest.mark.gpu
 
@@ -28,6 +32,9 @@ def test_auto_runs_the_selected_kernel(dev, opt, S, want):
     o, _, kind = attn.attn_fwd_auto(q, k, v, option_enabled=opt)
     device_status_ok()
     assert kind == want
+    # the policy's output against the fp64 oracle, element by element
+    o_ref, _ = oracle.attention(q.cpu(), k.cpu(), v.cpu(), layout=0, scale=1 / math.sqrt(64))
+    check_o(o, o_ref, q.dtype, f"attn_fwd_auto S={S} option={opt}")
     ref = (attn.attn_fwd(q, k, v, split=False)[0] if want == attn.ATTN_KERNEL_ONLINE
            else attn.attn_fwd_naive(q, k, v)[0])
     device_status_ok()

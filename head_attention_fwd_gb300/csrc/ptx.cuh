@@ -63,11 +63,11 @@ __device__ __forceinline__ void raise_abort(const WaitCtx& w, uint32_t code) {
   __threadfence_block();
 }
 
-// With honor_abort = false the wait ignores the abort flag (used to drain
-// copies and MMAs already in flight before a CTA winds down).  Out of line to
-// keep the polling loop out of hot code.
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtx& w,
-                                                   uint32_t code, bool honor_abort = true) {
+// The polling loop of a bounded wait.  With honor_abort = false the wait
+// ignores the abort flag (used to drain copies and MMAs already in flight
+// before a CTA winds down).
+__device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity, const WaitCtx& w, uint32_t code,
+                                          bool honor_abort = true) {
   const long long t0 = clock64();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -81,18 +81,28 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
   }
 }
 
+// The same loop out of line, to keep it out of hot code.  Kernels that move
+// registers between warpgroups (setmaxnreg) cannot call out-of-line code from
+// the regions with a changed register count and use the inline form.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtx& w,
+                                                   uint32_t code, bool honor_abort = true) {
+  return mbar_poll(bar, parity, w, code, honor_abort);
+}
+
 // Bounded wait for the phase with the given parity to complete.
+template <bool OUT_OF_LINE = true>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtx& w,
                                           uint32_t code) {
   if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, w, code);
+  return OUT_OF_LINE ? mbar_wait_slow(bar, parity, w, code) : mbar_poll(bar, parity, w, code);
 }
 
 // Same, with the outcome made uniform over the calling warp (every lane must
 // call it): false on every lane if any lane gave up.
+template <bool OUT_OF_LINE = true>
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const WaitCtx& w,
                                                uint32_t code) {
-  const bool ok = mbar_wait(bar, parity, w, code);
+  const bool ok = mbar_wait<OUT_OF_LINE>(bar, parity, w, code);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -351,6 +361,22 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
 
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Register split between warpgroups (setmaxnreg).  Every thread of a
+// warpgroup (four consecutive warps starting at a multiple of four) must
+// execute the same instruction, so a CTA using it must consist of whole
+// warpgroups.  .inc waits until the CTA's pool (threads x registers per
+// thread at launch) has room, so the shares must add up to no more than it.
+template <int N>
+__device__ __forceinline__ void reg_alloc() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg count");
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void reg_dealloc() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg count");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // --------------------------------------------------------- arithmetic ----

@@ -62,8 +62,9 @@ def parse_args():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-extra", action="store_true", help="skip the comparison / other-workload lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    ap.add_argument("--only", choices=["qkv", "naive", "mixed", "fused"],
-                    help="run only this path's calls (for profiling): the BERT-base projection + attention, "
+    ap.add_argument("--only", choices=["qkv", "qkv1", "naive", "mixed", "fused"],
+                    help="run only this path's calls (for profiling): the BERT-base projection + attention "
+                         "(qkv: two launches, qkv1: the single kernel), "
                          "the unfused two-pass path or the fp32-input path on the bench workload, or the fused "
                          "attention (attn_fwd with its balancing scratch) on --workload; prints its time per "
                          "call, not the benchmark line")
@@ -543,7 +544,18 @@ def run_extra(attn, w, sets, stream, dev):
     out["bert_base_qkv"] = {"tflops": fl / tg / 1e12, "ms": tg * 1e3,
                             "timing": "CUDA graph of 20 calls, replayed 10 times",
                             "tflops_eager": fl / (t / n) / 1e12, "ms_eager": t / n * 1e3,
-                            "flops": "projection 2*B*S*D*3D + attention 4*B*h*S^2*d"}
+                            "flops": "projection 2*B*S*D*3D + attention 4*B*h*S^2*d",
+                            "launches_per_call": 2}
+    # the same call as one kernel: projection tiles feed the attention on chip
+    for _ in range(3):
+        attn.qkv_proj_attn_fused(x, wq, wb.h, oo, stream=stream)
+    t = time_launches(lambda i: attn.qkv_proj_attn_fused(x, wq, wb.h, oo, stream=stream), n, stream)
+    tg = time_graph(lambda i: attn.qkv_proj_attn_fused(x, wq, wb.h, oo, stream=torch.cuda.current_stream()),
+                    20, 10)
+    out["bert_base_qkv_single_kernel"] = {"tflops": fl / tg / 1e12, "ms": tg * 1e3,
+                                          "timing": "CUDA graph of 20 calls, replayed 10 times",
+                                          "tflops_eager": fl / (t / n) / 1e12, "ms_eager": t / n * 1e3,
+                                          "launches_per_call": 1}
     wc = WORKLOADS["single_head_f32"]
     g = torch.Generator(device=dev).manual_seed(wc.seed)
     qq, kk, vv = (torch.randn(wc.shape(), generator=g, device=dev) for _ in range(3))
@@ -614,14 +626,17 @@ def run_only(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
-    if args.only == "qkv":
+    if args.only in ("qkv", "qkv1"):
         w = WORKLOADS["bert_base_qkv"]
         g = torch.Generator(device=dev).manual_seed(w.seed)
         x = torch.randn((w.B, w.S, w.D), generator=g, device=dev).to(w.torch_dtype)
         wq = (torch.randn((w.D, 3 * w.D), generator=g, device=dev) * w.w_std).to(w.torch_dtype)
         o = torch.empty((w.B, w.S, w.h, w.d), dtype=w.torch_dtype, device=dev)
         ws = torch.empty(attn.qkv_proj_attn_workspace_bytes(w.B, w.S, w.D, x.dtype), dtype=torch.uint8, device=dev)
-        call = lambda i: attn.qkv_proj_attn(x, wq, w.h, o, ws, stream=stream)
+        if args.only == "qkv":
+            call = lambda i: attn.qkv_proj_attn(x, wq, w.h, o, ws, stream=stream)
+        else:
+            call = lambda i: attn.qkv_proj_attn_fused(x, wq, w.h, o, stream=stream)
         flops = w.attn_flops + w.proj_flops
     elif args.only == "fused":
         from head_attention_fwd_gb300.inputs import make_qkv

@@ -12,6 +12,7 @@ Entry points (same names as the C ABI):
 * ``attn_fwd_mixed(q, k, v, ...)``  fp32 inputs, 16-bit output (converted once, then fused)
 * ``attn_fwd_naive(q, k, v, ...)``  unfused two-pass-softmax comparison path
 * ``qkv_proj_attn(x, w_qkv, h, ...)`` fused QKV projection, then attention
+* ``qkv_proj_attn_fused(x, w_qkv, h, ...)`` the same in one kernel (d = 64, S <= 512)
 * ``qkv_proj_attn_noalloc(x, w_qkv, h, ...)`` the same without a workspace argument
 * ``attn_get_device_status()``, ``attn_status_string(rc)``
 """
@@ -73,6 +74,8 @@ def lib() -> ctypes.CDLL:
             L.attn_fwd_naive_workspace_bytes.restype = sz
             L.qkv_proj_attn.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, vp, sz, vp]
             L.qkv_proj_attn.restype = ci
+            L.qkv_proj_attn_fused.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, vp]
+            L.qkv_proj_attn_fused.restype = ci
             L.qkv_proj_attn_noalloc.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, vp]
             L.qkv_proj_attn_noalloc.restype = ci
             L.qkv_proj_attn_workspace_bytes.argtypes = [ci, ci, ci, ci]
@@ -308,6 +311,21 @@ def qkv_proj_attn(x, w_qkv, h: int, o=None, workspace=None, *, stream=None):
     if rc:
         raise AttnError(rc, "qkv_proj_attn")
     return o, workspace
+
+
+def qkv_proj_attn_fused(x, w_qkv, h: int, o=None, *, stream=None):
+    """qkv_proj_attn in one kernel launch (d = D/h = 64, S <= 512): the projection
+    feeds the attention on chip, no workspace.  Returns o [B,S,h,d]."""
+    torch = _torch()
+    B, S, D = (int(n) for n in x.shape)
+    if o is None:
+        o = torch.empty((B, S, h, D // h), dtype=x.dtype, device=x.device)
+    _check_dense(x, w_qkv, o)
+    rc = lib().qkv_proj_attn_fused(_ptr(x), _ptr(w_qkv), _ptr(o), B, S, D, h, dtype_code(x.dtype),
+                                   _stream_ptr(stream))
+    if rc:
+        raise AttnError(rc, "qkv_proj_attn_fused")
+    return o
 
 
 def qkv_proj_attn_noalloc(x, w_qkv, h: int, o=None, *, stream=None):

@@ -21,7 +21,7 @@ LIB = os.path.join(HERE, "libattn_gb300.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 
 SOURCES = ["api.cu", "flash_fwd.cu", "simt_fwd.cu", "gemm.cu", "naive.cu", "noalloc.cu", "compare.cu",
-           "convert.cu"]
+           "convert.cu", "fused.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE,
                  "-Xptxas", "-warn-spills"]

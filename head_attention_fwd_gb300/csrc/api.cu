@@ -588,6 +588,44 @@ int qkv_proj_attn(const void* x, const void* w_qkv, void* o, int B, int S, int D
                    dtype, 3LL * D, D, ds, st);
 }
 
+int qkv_proj_attn_fused(const void* x, const void* w_qkv, void* o, int B, int S, int D, int h, int dtype,
+                        void* stream) {
+  int rc = attn::validate_qkv_proj(x, w_qkv, o, B, S, D, h, dtype);
+  if (rc) return rc;
+  if (D / h != 64 || S > 512) return ATTN_E_SHAPE;
+  DeviceState* ds = nullptr;
+  if ((rc = device_setup(&ds))) return rc;
+  attn::FusedLaunch a;
+  const cuuint64_t e = 2;
+  const CUtensorMapDataType dt =
+      dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  {  // X [B, S, D]: dims (D, S, B), box 64 x 128 x 1
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * e, static_cast<cuuint64_t>(S) * D * e};
+    cuuint32_t box[3] = {64, 128, 1}, estr[3] = {1, 1, 1};
+    if (g_encode(&a.tx, dt, 3, const_cast<void*>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return ATTN_E_DEVICE;
+  }
+  {  // W_qkv [D, 3D]: dims (3D, D), box 64 x 64
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(3LL * D), static_cast<cuuint64_t>(D)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(3LL * D) * e};
+    cuuint32_t box[2] = {64, 64}, estr[2] = {1, 1};
+    if (g_encode(&a.tw, dt, 2, const_cast<void*>(w_qkv), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return ATTN_E_DEVICE;
+  }
+  a.o = o;
+  a.B = B, a.S = S, a.H = h;
+  a.bf16 = dtype == ATTN_BF16;
+  a.scale = 1.0f / sqrtf(64.0f);
+  a.status = ds->status;
+  a.limit = wait_limit();
+  return to_rc(attn::launch_fused_qkv_attn(a, static_cast<cudaStream_t>(stream)));
+}
+
 const char* attn_status_string(int status) {
   switch (status) {
     case ATTN_OK: return "ATTN_OK";

@@ -61,6 +61,21 @@ FlashScratch flash_scratch_layout(int d, int grid);
 
 cudaError_t launch_flash_fwd(const FlashLaunch& a, const FlashPlan& plan, cudaStream_t st);
 
+// Single-kernel QKV projection + attention (fused.cu): one CTA per (batch,
+// head), d = 64, S <= 512.  tx: X [B, S, D] as a 3-d map (D, S, B), box
+// 64 x 128 x 1; tw: W_qkv [D, 3D] as a 2-d map (3D, D), box 64 x 64; both
+// 128-byte swizzled.  o: [B, S, H, 64].
+struct FusedLaunch {
+  CUtensorMap tx, tw;
+  void* o;
+  int B, S, H;
+  bool bf16;
+  float scale;
+  unsigned* status;
+  long long limit;
+};
+cudaError_t launch_fused_qkv_attn(const FusedLaunch& a, cudaStream_t st);
+
 struct SimtLaunch {
   const float *q, *k, *v;
   float* o;

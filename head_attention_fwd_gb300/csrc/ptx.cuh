@@ -11,7 +11,7 @@
 namespace attn {
 
 // Device status word codes (kernel id << 24 | role << 16 | tile index).
-enum KernelId : uint32_t { KID_FLASH = 1, KID_GEMM = 2, KID_SIMT = 3, KID_NAIVE = 4, KID_SELFTEST = 15 };
+enum KernelId : uint32_t { KID_FLASH = 1, KID_GEMM = 2, KID_SIMT = 3, KID_NAIVE = 4, KID_FUSED = 5, KID_SELFTEST = 15 };
 enum RoleId : uint32_t { ROLE_LOAD = 1, ROLE_MMA = 2, ROLE_SOFTMAX = 3, ROLE_EPILOGUE = 4 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -144,6 +144,13 @@ __device__ __forceinline__ bool flag_wait_warp(const unsigned long long* f, unsi
   }
 }
 
+// Makes this thread's earlier generic-proxy shared-memory writes visible to
+// the async proxy (TMA, tensor-core operand reads) once a later barrier
+// orders them.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- TMA ----
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
@@ -155,6 +162,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, 
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0,
+                                            int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
 }
 

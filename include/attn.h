@@ -249,6 +249,27 @@ int qkv_proj_attn(const void* x, const void* w_qkv, void* o, int B, int S, int D
 size_t qkv_proj_attn_workspace_bytes(int B, int S, int D, int dtype);
 
 /*
+ * qkv_proj_attn_fused -- the same result as qkv_proj_attn in ONE kernel
+ * launch, with the projection feeding the attention on chip: the fusion of
+ * "Transformer算子生态深度分析" §2.7 (算子层面的优化要点), the projected Q,
+ * K, V going straight into the attention instead of through memory.  One
+ * CTA per (batch, head) computes that head's K and V for all S positions
+ * (fp32 in tensor memory, then rounded to the 16-bit type in shared memory),
+ * then, 128 query rows at a time, Q and the online-softmax attention against
+ * them.  Nothing but X, W_qkv and O touches device memory: no workspace.
+ *
+ *   x, w_qkv, o, B, S, D, h, dtype, stream   as for qkv_proj_attn.
+ *
+ * Supported sizes: d = D / h = 64 and 1 <= S <= 512 (one head's K and V must
+ * fit in shared memory); other sizes return ATTN_E_SHAPE -- use
+ * qkv_proj_attn.  The result equals qkv_proj_attn's up to fp32 summation
+ * order (both round the projection to the 16-bit type before the attention).
+ * Errors: as qkv_proj_attn without the workspace checks.
+ */
+int qkv_proj_attn_fused(const void* x, const void* w_qkv, void* o, int B, int S, int D, int h, int dtype,
+                        void* stream);
+
+/*
  * qkv_proj_attn_noalloc -- qkv_proj_attn for callers that cannot allocate
  * device memory.  The pages have no counterpart to this entry point.
  *

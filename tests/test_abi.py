@@ -182,6 +182,24 @@ def test_qkv_proj_attn_validation_and_workspace(L):
     assert proj(ws=K) == E["ALIAS"]
 
 
+def test_qkv_proj_attn_fused_validation(L):
+    vp = ctypes.c_void_p
+
+    def fused(x=Q, w=K, o=O, B=8, S=512, D=768, h=12, dtype=1):
+        return L.qkv_proj_attn_fused(vp(x), vp(w), vp(o), B, S, D, h, dtype, vp(0))
+
+    assert fused(x=None) == E["NULL"]
+    assert fused(dtype=0) == E["DTYPE"]
+    assert fused(S=513) == E["SHAPE"]        # one head's K and V must fit in shared memory
+    assert fused(h=6) == E["SHAPE"]          # d = 128: not supported by the single kernel
+    assert fused(D=770) == E["SHAPE"]
+    assert fused(S=0) == E["SHAPE"]
+    assert fused(w=K + 8) == E["ALIGN"]
+    assert fused(o=Q + 1024) == E["ALIAS"]
+    if not torch.cuda.is_available():
+        assert fused() == E["DEVICE"]
+
+
 def test_qkv_proj_attn_noalloc_checks_arguments_before_the_scratch_limit(L):
     """A bad argument is reported as such even on a problem too large for the
     fixed scratch; only a valid problem that is too large gets the limit code."""

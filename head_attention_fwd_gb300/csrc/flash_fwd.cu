@@ -7,7 +7,7 @@
 // ("WebGPU 算子优化：QKV 内存合并与 FlashAttention 分块计算",
 // §FlashAttention 分块计算原理与浏览器适配, gives the same merge rule).
 //
-// GB300 mapping (at most one CTA per SM, 12 warps, 192 KB of shared memory):
+// GB300 mapping (at most one CTA per SM, 11 warps, 192 KB of shared memory):
 //   * work item = one (batch, head) and two 128-row Q tiles -- "ping-pong":
 //     while one tile's softmax runs on the CUDA cores, the tensor cores work
 //     on the other tile;
@@ -51,11 +51,7 @@
 //     O_t of the next segment is started only after the softmax warps have
 //     read this segment's O_t (barrier o_free);
 //   * each issuer warp issues from a converged warp (elect.sync picks the
-//     lane), so descriptors stay warp-uniform;
-//   * registers: the CTA is three whole warpgroups so that setmaxnreg can
-//     move registers from warpgroup 2 (producer, issuers and a spare warp,
-//     80 each) to the softmax warpgroups (208 each) -- a row of S plus P
-//     stays in registers without spills.
+//     lane), so descriptors stay warp-uniform.
 // Every wait is bounded: a pipeline stall records a code in the device
 // status word and the CTA winds down instead of hanging.
 
@@ -97,14 +93,7 @@ struct Cfg {
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t OFF_WORK = OFF_MISC + 16;     // CtaWork
   static constexpr uint32_t SMEM = OFF_WORK + 32 + 1024;   // + slack for 1024-byte alignment
-  static constexpr int THREADS = 384;                      // three whole warpgroups
-  // Registers per thread after the split: the softmax warpgroups hold a row
-  // of S (128 values) and P; warpgroup 2 (producer, issuers, one spare warp)
-  // needs few.  The launch gives 168 per thread (three warps per SM
-  // sub-partition share its 16 K registers); the shares must fit that pool.
-  static constexpr int REG_SOFTMAX = 208;
-  static constexpr int REG_OTHER = 88;
-  static constexpr int REG_LAUNCH = 168;
+  static constexpr int THREADS = 352;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_S = 0;                     // + 128 t
   static constexpr uint32_t COL_O = 256;                   // + D t
@@ -127,9 +116,6 @@ struct Cfg {
   __host__ __device__ static constexpr int bar_ofree(int t) { return TB + 12 + t; }
   __host__ __device__ static constexpr uint32_t col_p(int t) { return COL_P + (SEP_P ? 64u : 128u) * t; }
 };
-static_assert(8 * Cfg<64>::REG_SOFTMAX + 4 * Cfg<64>::REG_OTHER <= 12 * Cfg<64>::REG_LAUNCH &&
-                  8 * Cfg<128>::REG_SOFTMAX + 4 * Cfg<128>::REG_OTHER <= 12 * Cfg<128>::REG_LAUNCH,
-              "register split exceeds the launch pool");
 static_assert(Cfg<128>::SMEM <= 227 * 1024, "shared memory budget");
 static_assert(Cfg<64>::SMEM <= 227 * 1024, "shared memory budget");
 static_assert(Cfg<64>::COL_P + 128 <= 512, "tensor memory budget");
@@ -269,7 +255,7 @@ __device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
 
 // MODE (see Mode): only MODE_SPLIT carries the piece / merge code.
 template <int D, bool BF16, bool GROUPED, int MODE>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(352, 1)
     flash_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ Params p) {
   using C = Cfg<D>;
@@ -349,11 +335,6 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_slot, 0);
   const WaitCtx wc{abort_flag, p.status, p.limit};
   const bool skip = *abort_flag != 0;
-  // Warpgroup-uniform: warps 0-7 (softmax) take registers, 8-11 give them up.
-  if (warp >= 8)
-    reg_dealloc<C::REG_OTHER>();
-  else
-    reg_alloc<C::REG_SOFTMAX>();
 
   if (skip) {
     // nothing
@@ -384,7 +365,7 @@ __global__ void __launch_bounds__(384, 1)
       const ItemPos ip = item_pos(p, sg.item);
       const int qs = kq % C::NQB;
       if (kq >= C::NQB)
-        ok = mbar_wait_warp<false>(bar(C::bar_qempty(qs)), ((kq / C::NQB) - 1) & 1, wc, code_of(ROLE_LOAD, it));
+        ok = mbar_wait_warp(bar(C::bar_qempty(qs)), ((kq / C::NQB) - 1) & 1, wc, code_of(ROLE_LOAD, it));
       if (!ok) break;
       if (lane == 0) {
         mbar_expect_tx(bar(C::bar_qfull(qs)), C::QSET);
@@ -396,7 +377,7 @@ __global__ void __launch_bounds__(384, 1)
       ++kq;
       for (int j = sg.jb; j < sg.je; ++j, ++it) {
         const uint32_t s = it % C::STAGES, u = it / C::STAGES;
-        if (u > 0) ok = mbar_wait_warp<false>(bar(C::bar_kempty(s)), (u - 1) & 1, wc, code_of(ROLE_LOAD, it));
+        if (u > 0) ok = mbar_wait_warp(bar(C::bar_kempty(s)), (u - 1) & 1, wc, code_of(ROLE_LOAD, it));
         if (!ok) break;
         if (lane == 0) {
           mbar_expect_tx(bar(C::bar_kfull(s)), C::TILE);
@@ -405,7 +386,7 @@ __global__ void __launch_bounds__(384, 1)
                  j * C::BN, ip);
         }
         issued_k = it + 1;
-        if (u > 0) ok = mbar_wait_warp<false>(bar(C::bar_vempty(s)), (u - 1) & 1, wc, code_of(ROLE_LOAD, it));
+        if (u > 0) ok = mbar_wait_warp(bar(C::bar_vempty(s)), (u - 1) & 1, wc, code_of(ROLE_LOAD, it));
         if (!ok) break;
         if (lane == 0) {
           mbar_expect_tx(bar(C::bar_vfull(s)), C::TILE);
@@ -419,11 +400,11 @@ __global__ void __launch_bounds__(384, 1)
     if (!ok) {
       // Let the copies already in flight land before the CTA can exit.
       for (uint32_t x = issued_k > C::STAGES ? issued_k - C::STAGES : 0; x < issued_k; ++x)
-        mbar_poll(bar(C::bar_kfull(x % C::STAGES)), (x / C::STAGES) & 1, wc, 0, false);
+        mbar_wait_slow(bar(C::bar_kfull(x % C::STAGES)), (x / C::STAGES) & 1, wc, 0, false);
       for (uint32_t x = issued_v > C::STAGES ? issued_v - C::STAGES : 0; x < issued_v; ++x)
-        mbar_poll(bar(C::bar_vfull(x % C::STAGES)), (x / C::STAGES) & 1, wc, 0, false);
+        mbar_wait_slow(bar(C::bar_vfull(x % C::STAGES)), (x / C::STAGES) & 1, wc, 0, false);
       for (int x = kq > C::NQB ? kq - C::NQB : 0; x < kq; ++x)
-        mbar_poll(bar(C::bar_qfull(x % C::NQB)), (x / C::NQB) & 1, wc, 0, false);
+        mbar_wait_slow(bar(C::bar_qfull(x % C::NQB)), (x / C::NQB) & 1, wc, 0, false);
     }
     } else if (warp == 9 || (C::ISSUERS == 2 && warp == 10)) {
     // ------------------------------------------------ tcgen05 issuer(s) ----
@@ -450,7 +431,7 @@ __global__ void __launch_bounds__(384, 1)
     };
     auto commit = [&](int i) { mma_commit_elect(bar(i)); };
     auto wait = [&](int i, uint32_t parity, uint32_t j) {
-      return mbar_wait_warp<false>(bar(i), parity, wc, code_of(ROLE_MMA, j));
+      return mbar_wait_warp(bar(i), parity, wc, code_of(ROLE_MMA, j));
     };
     bool ok = true;
     if constexpr (C::ISSUERS == 2) {
@@ -496,7 +477,7 @@ __global__ void __launch_bounds__(384, 1)
       if (!ok) {
         // Wait for the MMAs already issued before tensor memory is released.
         commit(C::bar_drain(t));
-        mbar_poll(bar(C::bar_drain(t)), 0, wc, 0, false);
+        mbar_wait_slow(bar(C::bar_drain(t)), 0, wc, 0, false);
       }
     } else {
       // One issuer, tiles in alternation; P overwrites S, so the next S_t is
@@ -553,7 +534,7 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (!ok) {
         commit(C::bar_drain(0));
-        mbar_poll(bar(C::bar_drain(0)), 0, wc, 0, false);
+        mbar_wait_slow(bar(C::bar_drain(0)), 0, wc, 0, false);
       }
     }
     }
@@ -571,7 +552,7 @@ __global__ void __launch_bounds__(384, 1)
     float l = 0.f;            // running sum of p
     bool ok = true;
     auto wait = [&](int i, uint32_t parity, uint32_t j) {
-      return mbar_wait_warp<false>(bar(i), parity, wc, code_of(ROLE_SOFTMAX, j));
+      return mbar_wait_warp(bar(i), parity, wc, code_of(ROLE_SOFTMAX, j));
     };
     uint32_t r[4][32];  // this thread's row of S_t
     // Ragged key tail: the columns from `valid` on do not exist.  They are set
@@ -909,12 +890,6 @@ __global__ void __launch_bounds__(384, 1)
     if (SPLIT && ok && piece_pending) publish_piece();
   }
 
-  // Back to the launch share before the paths join (warpgroup-uniform; the
-  // softmax warps release first, so warpgroup 2's request can be granted).
-  if (warp >= 8)
-    reg_alloc<C::REG_LAUNCH>();
-  else
-    reg_dealloc<C::REG_LAUNCH>();
   tc_fence_before();
   __syncthreads();
   if (warp == 9) {
@@ -927,15 +902,6 @@ template <int D, bool BF16, bool GROUPED, int MODE>
 cudaError_t launch_impl(const FlashLaunch& a, const FlashPlan& plan, cudaStream_t st) {
   using C = Cfg<D>;
   auto kern = flash_fwd_kernel<D, BF16, GROUPED, MODE>;
-  // The register split can only be granted if the kernel was compiled with
-  // the full launch share per thread (a smaller pool would make the
-  // softmax warps' setmaxnreg.inc wait forever): check once per instance.
-  static const int regs_ok = [&] {
-    cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return 0;
-    return fa.numRegs * C::THREADS >= 32 * (8 * C::REG_SOFTMAX + 4 * C::REG_OTHER) ? 1 : 0;
-  }();
-  if (!regs_ok) return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   Params p{};

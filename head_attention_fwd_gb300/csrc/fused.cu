@@ -7,31 +7,37 @@
 // [D, 3D] weight (columns [0, D) give Q, [D, 2D) K, [2D, 3D) V, head-major).
 // The attention itself is the online softmax of §2.6, as in flash_fwd.cu.
 //
-// Scope: d = 64 and S <= 512 -- one head's K and V for the whole sequence
-// then fit in shared memory (128 KB) and their fp32 accumulators in tensor
+// Scope: d = 64 and S <= 512 -- one head's Q, K and V for the whole sequence
+// then fit in shared memory (192 KB) and their fp32 accumulators in tensor
 // memory.  That is the short-sequence, BERT-like regime in which the
 // projection dominates; longer sequences use the two-launch qkv_proj_attn.
 //
-// One CTA per (batch, head), 12 warps (three whole warpgroups):
+// One CTA per (batch, head), 12 warps:
 //   warp 8     TMA producer;
 //   warp 9     tcgen05 issuer;
 //   warps 0-7  epilogue / softmax: warpgroup t owns query block t of the
 //              current pair, one thread per row (tensor-memory lane);
 //   warps 10-11 spare.
-// Phase A  [K | V] = X_b · [W_k,h | W_v,h] for all S rows: one N = 128 MMA per
-//          16-wide k-step and 128-row block (K in the accumulator's first 64
-//          columns, V in the next 64), the k-chunk's weight tile shared by
-//          all row blocks.  The epilogue warps round the accumulators to the
-//          16-bit type and store them into shared memory in the 128-byte-
-//          swizzled layout that TMA would have produced, K row-major by key
-//          (B operand of Q·K^T) and V row-major by key (B operand of P·V).
-// Phase B  for each pair of 128-row query blocks: Q = X_b[rows] · W_q,h into
-//          tensor memory (the columns S of each block uses later), rounded
-//          into shared memory the same way, then the attention of the two
-//          blocks against the shared-memory K and V: the tensor cores compute
-//          one block's products while the softmax warps of the other run.
-// Tensor memory: phase A [K|V] of row block r in columns 128r.. (512 for
-// S = 512); phase B S0 | S1 | O0 | O1 | P0 | P1 (128+128+64+64+64+64).
+// Phase Q   Q = X_b · W_q,h for all S rows: one N = 64 MMA per 16-wide k-step
+//           and 128-row block, each k-chunk of X loaded once for all blocks
+//           and the weight chunk shared by them; the epilogue warps round the
+//           accumulators to the 16-bit type into shared memory, in the
+//           128-byte-swizzled layout that TMA would have produced (the A
+//           operand of Q·K^T).
+// Phase KV  [K | V] = X_b · [W_k,h | W_v,h]: one N = 128 MMA per k-step and
+//           block (K in the accumulator's first 64 columns, V in the next 64),
+//           rounded into shared memory the same way (K: B operand of Q·K^T,
+//           V: B operand of P·V, both row-major by key).
+// Attention for each pair of 128-row query blocks against the shared-memory
+//           K and V: the tensor cores compute one block's products while the
+//           softmax warps of the other run.  The output rows leave through
+//           the pair's Q tiles (free once its Q·K^T products are done) as
+//           whole 128-byte row segments.
+// Tensor memory: phase Q block r in columns 64r..; phase KV block r in
+// columns 128r..; attention S0 | S1 | O0 | O1 | P0 | P1 (128+128+64+64+64+64).
+// Shared memory: Q tiles | K tiles | V tiles (64 KB each); the projection
+// ring (two stages of 80 KB) overlaps the K and V tiles, which are written
+// only once every load has been consumed.
 // Every wait is bounded; a stall records a code in the device status word and
 // the CTA winds down instead of hanging.
 
@@ -45,34 +51,32 @@ constexpr float kLog2eF = 1.4426950408889634f;
 constexpr float kThresholdF = 8.0f;  // lazy rescale: move the reference when the max grows by > 2^8
 
 struct FCfg {
-  static constexpr int MAXT = 4;          // 128-row blocks (S <= 512)
+  static constexpr int MAXT = 4;                         // 128-row blocks (S <= 512)
   static constexpr uint32_t TILE = 128 * 128;            // 128 rows x 64 elements x 2 bytes
   static constexpr uint32_t WCH = 64 * 128;              // weight chunk: 64 k-rows x 64 columns
-  static constexpr uint32_t OFF_K = 0;                   // K tiles (phase B)
-  static constexpr uint32_t OFF_V = MAXT * TILE;         // V tiles (phase B)
-  static constexpr uint32_t OFF_A = 0;                   // phase-A ring (aliases K, V, B ring)
-  static constexpr uint32_t ASTAGE = MAXT * TILE + 2 * WCH;   // X tiles of all row blocks + W_k, W_v chunks
-  static constexpr uint32_t OFF_B = 2 * MAXT * TILE;     // phase-B ring; Q tiles alias its stage 0
-  static constexpr uint32_t BSTAGE = 2 * TILE + WCH;     // X tiles of the two query blocks + W_q chunk
-  static constexpr uint32_t OFF_BAR = OFF_B + 2 * BSTAGE;
-  static constexpr int NBAR = 24;
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_K = MAXT * TILE;
+  static constexpr uint32_t OFF_V = 2 * MAXT * TILE;
+  static constexpr uint32_t OFF_R = MAXT * TILE;         // projection ring (overlaps K, V)
+  static constexpr uint32_t STAGE = MAXT * TILE + 2 * WCH;  // X tiles of every block + one or two weight chunks
+  static constexpr uint32_t OFF_BAR = OFF_R + 2 * STAGE;
+  static constexpr int NBAR = 20;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t SMEM = OFF_MISC + 16 + 1024;
   static constexpr int THREADS = 384;
   static constexpr uint32_t COL_O = 256, COL_P = 384;
   // barriers
-  __host__ __device__ static constexpr int afull(int s) { return s; }
-  __host__ __device__ static constexpr int aempty(int s) { return 2 + s; }
-  __host__ __device__ static constexpr int bfull(int s) { return 4 + s; }
-  __host__ __device__ static constexpr int bempty(int s) { return 6 + s; }
-  static constexpr int KVACC = 8, KVREADY = 9, QACC = 10, QREADY = 11, QFREE = 12, DRAIN = 13;
-  __host__ __device__ static constexpr int sfull(int t) { return 14 + t; }
-  __host__ __device__ static constexpr int sconsumed(int t) { return 16 + t; }
-  __host__ __device__ static constexpr int pready(int t) { return 18 + t; }
-  __host__ __device__ static constexpr int oready(int t) { return 20 + t; }
-  __host__ __device__ static constexpr int ofree(int t) { return 22 + t; }
+  __host__ __device__ static constexpr int full(int s) { return s; }
+  __host__ __device__ static constexpr int empty(int s) { return 2 + s; }
+  static constexpr int QACC = 4, QREADY = 5, KVACC = 6, KVREADY = 7, QFREE = 8, DRAIN = 9;
+  __host__ __device__ static constexpr int sfull(int t) { return 10 + t; }
+  __host__ __device__ static constexpr int sconsumed(int t) { return 12 + t; }
+  __host__ __device__ static constexpr int pready(int t) { return 14 + t; }
+  __host__ __device__ static constexpr int oready(int t) { return 16 + t; }
+  __host__ __device__ static constexpr int ofree(int t) { return 18 + t; }
 };
-static_assert(FCfg::OFF_A + 2 * FCfg::ASTAGE <= FCfg::OFF_BAR, "phase-A ring inside the buffers");
+static_assert(FCfg::OFF_R + 2 * FCfg::STAGE <= FCfg::OFF_BAR && FCfg::OFF_V + FCfg::MAXT * FCfg::TILE <= FCfg::OFF_BAR,
+              "buffers inside the shared-memory budget");
 static_assert(FCfg::SMEM <= 227 * 1024, "shared memory budget");
 
 struct FParams {
@@ -125,15 +129,13 @@ __global__ void __launch_bounds__(384, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(C::afull(s)), 1);
-      mbar_init(bar(C::aempty(s)), 1);
-      mbar_init(bar(C::bfull(s)), 1);
-      mbar_init(bar(C::bempty(s)), 1);
+      mbar_init(bar(C::full(s)), 1);
+      mbar_init(bar(C::empty(s)), 1);
     }
-    mbar_init(bar(C::KVACC), 1);
-    mbar_init(bar(C::KVREADY), 256);
     mbar_init(bar(C::QACC), 1);
     mbar_init(bar(C::QREADY), 256);
+    mbar_init(bar(C::KVACC), 1);
+    mbar_init(bar(C::KVREADY), 256);
     mbar_init(bar(C::QFREE), 1);
     mbar_init(bar(C::DRAIN), 1);
     for (int t = 0; t < 2; ++t) {
@@ -164,137 +166,100 @@ __global__ void __launch_bounds__(384, 1)
   if (skip) {
   } else if (warp == 8) {
     // ------------------------------------------------------ TMA producer ----
+    // Ring stage s at OFF_R + s·STAGE: the X tiles of every block for one
+    // k-chunk, then the weight chunk(s): W_q (phase Q) or W_k, W_v (phase KV).
     if (lane == 0) {
       prefetch_tmap(&tx);
       prefetch_tmap(&tw);
     }
-    auto wait = [&](int i, uint32_t parity, uint32_t j) {
-      return mbar_wait_warp<false>(bar(i), parity, wc, fcode(ROLE_LOAD, j));
-    };
     bool ok = true;
-    int issued_a = 0, issued_b = 0;
-    // Phase A: per k-chunk, the X tiles of every row block and the W_k, W_v chunks.
-    for (int kc = 0; kc < p.nkc && ok; ++kc) {
-      const int s = kc & 1, u = kc >> 1;
-      if (u > 0 && !(ok = wait(C::aempty(s), (u - 1) & 1, kc))) break;
-      if (lane == 0) {
-        const uint32_t st = sb + C::OFF_A + s * C::ASTAGE;
-        mbar_expect_tx(bar(C::afull(s)), nt * C::TILE + 2 * C::WCH);
-        for (int r = 0; r < nt; ++r) tma_load_3d(st + r * C::TILE, &tx, bar(C::afull(s)), kc * 64, r * 128, b);
-        tma_load_2d(st + C::MAXT * C::TILE, &tw, bar(C::afull(s)), p.D + hh * 64, kc * 64);
-        tma_load_2d(st + C::MAXT * C::TILE + C::WCH, &tw, bar(C::afull(s)), 2 * p.D + hh * 64, kc * 64);
-      }
-      issued_a = kc + 1;
-    }
-    // The phase-B ring overlaps phase-A stage 1: start only once both
-    // phase-A stages have been consumed.
-    for (int g = issued_a - 2 < 0 ? 0 : issued_a - 2; ok && g < issued_a; ++g)
-      ok = wait(C::aempty(g & 1), (g >> 1) & 1, g);
-    // Phase B: per pair, per k-chunk, the X tiles of the two query blocks and the W_q chunk.
-    int gb = 0;
-    for (int pr = 0; pr < npair && ok; ++pr) {
-      if (pr > 0 && !(ok = wait(C::QFREE, (pr - 1) & 1, pr))) break;  // Q tiles alias stage 0
-      for (int kc = 0; kc < p.nkc; ++kc, ++gb) {
-        const int s = gb & 1, u = gb >> 1;
-        if (u > 0 && !(ok = wait(C::bempty(s), (u - 1) & 1, gb))) break;
+    int g = 0;  // ring loads issued (both phases)
+    for (int ph = 0; ph < 2 && ok; ++ph) {
+      for (int kc = 0; kc < p.nkc; ++kc, ++g) {
+        const int s = g & 1, u = g >> 1;
+        if (u > 0 && !(ok = mbar_wait_warp(bar(C::empty(s)), (u - 1) & 1, wc, fcode(ROLE_LOAD, g)))) break;
         if (lane == 0) {
-          const uint32_t st = sb + C::OFF_B + s * C::BSTAGE;
-          mbar_expect_tx(bar(C::bfull(s)), C::BSTAGE);
-          tma_load_3d(st, &tx, bar(C::bfull(s)), kc * 64, (2 * pr) * 128, b);
-          tma_load_3d(st + C::TILE, &tx, bar(C::bfull(s)), kc * 64, (2 * pr + 1) * 128, b);
-          tma_load_2d(st + 2 * C::TILE, &tw, bar(C::bfull(s)), hh * 64, kc * 64);
+          const uint32_t st = sb + C::OFF_R + s * C::STAGE;
+          mbar_expect_tx(bar(C::full(s)), nt * C::TILE + (ph == 0 ? 1 : 2) * C::WCH);
+          for (int r = 0; r < nt; ++r) tma_load_3d(st + r * C::TILE, &tx, bar(C::full(s)), kc * 64, r * 128, b);
+          if (ph == 0) {
+            tma_load_2d(st + C::MAXT * C::TILE, &tw, bar(C::full(s)), hh * 64, kc * 64);
+          } else {
+            tma_load_2d(st + C::MAXT * C::TILE, &tw, bar(C::full(s)), p.D + hh * 64, kc * 64);
+            tma_load_2d(st + C::MAXT * C::TILE + C::WCH, &tw, bar(C::full(s)), 2 * p.D + hh * 64, kc * 64);
+          }
         }
-        issued_b = gb + 1;
       }
     }
     if (!ok) {  // let the copies in flight land before the CTA can exit
-      for (int g = issued_a - 2 < 0 ? 0 : issued_a - 2; g < issued_a; ++g)
-        mbar_poll(bar(C::afull(g & 1)), (g >> 1) & 1, wc, 0, false);
-      for (int g = issued_b - 2 < 0 ? 0 : issued_b - 2; g < issued_b; ++g)
-        mbar_poll(bar(C::bfull(g & 1)), (g >> 1) & 1, wc, 0, false);
+      for (int q = g - 2 < 0 ? 0 : g - 2; q < g; ++q)
+        mbar_wait_slow(bar(C::full(q & 1)), (q >> 1) & 1, wc, 0, false);
     }
   } else if (warp == 9) {
     // ------------------------------------------------- tcgen05 issuer ----
-    constexpr uint32_t id_kv = idesc_f16(128, 128, BF16, false, true);   // X · [W_k | W_v]
     constexpr uint32_t id_q = idesc_f16(128, 64, BF16, false, true);     // X · W_q
+    constexpr uint32_t id_kv = idesc_f16(128, 128, BF16, false, true);   // X · [W_k | W_v]
     constexpr uint32_t id_qk = idesc_f16(128, 128, BF16, false, false);  // Q · K^T
     constexpr uint32_t id_pv = idesc_f16(128, 64, BF16, false, true);    // P · V
     auto wait = [&](int i, uint32_t parity, uint32_t j) {
-      return mbar_wait_warp<false>(bar(i), parity, wc, fcode(ROLE_MMA, j));
+      return mbar_wait_warp(bar(i), parity, wc, fcode(ROLE_MMA, j));
     };
     auto commit = [&](int i) { mma_commit_elect(bar(i)); };
     bool ok = true;
-    // Phase A
-    for (int kc = 0; kc < p.nkc && ok; ++kc) {
-      const int s = kc & 1;
-      if (!(ok = wait(C::afull(s), (kc >> 1) & 1, kc))) break;
-      tc_fence_after();
-      const uint32_t st = sb + C::OFF_A + s * C::ASTAGE;
-      const uint64_t dw = sdesc_sw128(st + C::MAXT * C::TILE, C::WCH, 1024);
-      for (int r = 0; r < nt; ++r) {
-        const uint64_t dx = sdesc_sw128(st + r * C::TILE, 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ss_elect(tmem + r * 128, dx + ((kk * 32) >> 4), dw + ((kk * 2048) >> 4), id_kv,
-                       (kc > 0 || kk > 0) ? 1u : 0u);
-      }
-      commit(C::aempty(s));
-    }
-    if (ok) commit(C::KVACC);
-    if (ok) ok = wait(C::KVREADY, 0, 0);
-    // Phase B
-    int gb = 0;
-    uint32_t n = 0;  // key tiles of both blocks done (attention barrier phases)
-    for (int pr = 0; pr < npair && ok; ++pr) {
-      for (int kc = 0; kc < p.nkc; ++kc, ++gb) {
-        const int s = gb & 1;
-        if (!(ok = wait(C::bfull(s), (gb >> 1) & 1, gb))) break;
+    int g = 0;
+    for (int ph = 0; ph < 2 && ok; ++ph) {
+      // Phase KV overwrites the Q accumulators: only once they are in shared memory.
+      if (ph == 1 && !(ok = wait(C::QREADY, 0, 0))) break;
+      for (int kc = 0; kc < p.nkc; ++kc, ++g) {
+        const int s = g & 1;
+        if (!(ok = wait(C::full(s), (g >> 1) & 1, g))) break;
         tc_fence_after();
-        const uint32_t st = sb + C::OFF_B + s * C::BSTAGE;
-        const uint64_t dw = sdesc_sw128(st + 2 * C::TILE, C::WCH, 1024);
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const uint64_t dx = sdesc_sw128(st + t * C::TILE, 16, 1024);
+        const uint32_t st = sb + C::OFF_R + s * C::STAGE;
+        const uint64_t dw = sdesc_sw128(st + C::MAXT * C::TILE, C::WCH, 1024);
+        for (int r = 0; r < nt; ++r) {
+          const uint64_t dx = sdesc_sw128(st + r * C::TILE, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ss_elect(tmem + t * 128, dx + ((kk * 32) >> 4), dw + ((kk * 2048) >> 4), id_q,
-                         (kc > 0 || kk > 0) ? 1u : 0u);
+            mma_ss_elect(tmem + r * (ph == 0 ? 64 : 128), dx + ((kk * 32) >> 4), dw + ((kk * 2048) >> 4),
+                         ph == 0 ? id_q : id_kv, (kc > 0 || kk > 0) ? 1u : 0u);
         }
-        commit(C::bempty(s));
+        commit(C::empty(s));
       }
-      if (!ok) break;
-      commit(C::QACC);
-      if (!(ok = wait(C::QREADY, pr & 1, pr))) break;
+      if (ok) commit(ph == 0 ? C::QACC : C::KVACC);
+    }
+    if (ok) ok = wait(C::KVREADY, 0, 0);
+    auto qk = [&](int t, int qb, int j) {  // S_t = Q_qb · K_j^T
+      const uint64_t dq = sdesc_sw128(sb + C::OFF_Q + qb * C::TILE, 16, 1024);
+      const uint64_t dk = sdesc_sw128(sb + C::OFF_K + j * C::TILE, 16, 1024);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_ss_elect(tmem + t * 128, dq + ((kk * 32) >> 4), dk + ((kk * 32) >> 4), id_qk, kk > 0 ? 1u : 0u);
+    };
+    auto pv = [&](int t, int j) {  // O_t (+)= P_t · V_j
+      const uint64_t dv = sdesc_sw128(sb + C::OFF_V + j * C::TILE, C::TILE, 1024);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ts_elect(tmem + C::COL_O + t * 64, tmem + C::COL_P + t * 64 + kk * 8, dv + ((kk * 2048) >> 4), id_pv,
+                     (j > 0 || kk > 0) ? 1u : 0u);
+    };
+    uint32_t n = 0;  // key tiles of both blocks done (attention barrier phases)
+    for (int pr = 0; pr < npair && ok; ++pr) {
       tc_fence_after();
-      auto qk = [&](int t, int j) {  // S_t = Q_t · K_j^T
-        const uint64_t dq = sdesc_sw128(sb + C::OFF_B + t * C::TILE, 16, 1024);
-        const uint64_t dk = sdesc_sw128(sb + C::OFF_K + j * C::TILE, 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ss_elect(tmem + t * 128, dq + ((kk * 32) >> 4), dk + ((kk * 32) >> 4), id_qk, kk > 0 ? 1u : 0u);
-      };
-      auto pv = [&](int t, int j) {  // O_t (+)= P_t · V_j
-        const uint64_t dv = sdesc_sw128(sb + C::OFF_V + j * C::TILE, C::TILE, 1024);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts_elect(tmem + C::COL_O + t * 64, tmem + C::COL_P + t * 64 + kk * 8, dv + ((kk * 2048) >> 4),
-                       id_pv, (j > 0 || kk > 0) ? 1u : 0u);
-      };
-      qk(0, 0);
+      qk(0, 2 * pr, 0);
       commit(C::sfull(0));
-      qk(1, 0);
+      qk(1, 2 * pr + 1, 0);
       commit(C::sfull(1));
       for (int j = 0; j < nt && ok; ++j, ++n) {
         for (int t = 0; t < 2; ++t) {
           if (!(ok = wait(C::sconsumed(t), n & 1, n))) break;
           if (j + 1 < nt) {
             tc_fence_after();
-            qk(t, j + 1);
+            qk(t, 2 * pr + t, j + 1);
             commit(C::sfull(t));
           }
         }
         if (!ok) break;
-        if (j + 1 == nt) commit(C::QFREE);  // every Q·K^T of this pair issued: Q tiles free once done
+        if (j + 1 == nt) commit(C::QFREE);  // the pair's Q tiles are free once these products are done
         for (int t = 0; t < 2; ++t) {
           if (!(ok = wait(C::pready(t), n & 1, n))) break;
           if (j == 0 && pr > 0 && !(ok = wait(C::ofree(t), (pr - 1) & 1, n))) break;
@@ -306,20 +271,42 @@ __global__ void __launch_bounds__(384, 1)
     }
     if (!ok) {
       commit(C::DRAIN);
-      mbar_poll(bar(C::DRAIN), 0, wc, 0, false);
+      mbar_wait_slow(bar(C::DRAIN), 0, wc, 0, false);
     }
   } else if (warp < 8) {
     // -------------------------------------- epilogue / softmax warps 0-7 ----
-    const int t = static_cast<int>(warp) >> 2;   // phase A: 0 = K part, 1 = V part; phase B: query block
+    const int t = static_cast<int>(warp) >> 2;
     const uint32_t wq = warp & 3u;
-    const int r = static_cast<int>(wq * 32u + lane);  // row within the 128-row block
+    const int r = static_cast<int>(wq * 32u + lane);  // row within a 128-row block
     const uint32_t lane_off = (wq * 32u) << 16;
     auto wait = [&](int i, uint32_t parity, uint32_t j) {
-      return mbar_wait_warp<false>(bar(i), parity, wc, fcode(ROLE_SOFTMAX, j));
+      return mbar_wait_warp(bar(i), parity, wc, fcode(ROLE_SOFTMAX, j));
     };
-    bool ok = wait(C::KVACC, 0, 0);
+    // Phase Q epilogue: warpgroup t rounds blocks t and t + 2 (a block past the
+    // sequence that a pair still needs gets zeros).
+    bool ok = wait(C::QACC, 0, 0);
     if (ok) {
-      // Phase A epilogue: row r of every row block, K (t = 0) or V (t = 1) half.
+      tc_fence_after();
+      for (int qb = t; qb < 2 * npair; qb += 2) {
+        uint32_t a[32], c[32];
+        if (qb < nt) {
+          tmem_ld32(tmem + lane_off + qb * 64, a);
+          tmem_ld32(tmem + lane_off + qb * 64 + 32, c);
+          tmem_ld_wait(a);
+          tmem_ld_wait(c);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) a[i] = c[i] = 0u;
+        }
+        store_row_swizzled<BF16>(smem + C::OFF_Q + qb * C::TILE, r, a, c);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(C::QREADY));
+      ok = wait(C::KVACC, 0, 0);
+    }
+    if (ok) {
+      // Phase KV epilogue: row r of every block, K (t = 0) or V (t = 1) half.
       tc_fence_after();
       uint8_t* dst = smem + (t == 0 ? C::OFF_K : C::OFF_V);
       for (int rb = 0; rb < nt; ++rb) {
@@ -342,20 +329,6 @@ __global__ void __launch_bounds__(384, 1)
     uint32_t n = 0;
     uint32_t s_row[4][32];
     for (int pr = 0; pr < npair && ok; ++pr) {
-      // Q of block t of this pair: accumulator -> 16-bit -> Q tile in shared memory.
-      if (!(ok = wait(C::QACC, pr & 1, pr))) break;
-      tc_fence_after();
-      {
-        uint32_t a[32], c[32];
-        tmem_ld32(tS, a);
-        tmem_ld32(tS + 32, c);
-        tmem_ld_wait(a);
-        tmem_ld_wait(c);
-        store_row_swizzled<BF16>(smem + C::OFF_B + t * C::TILE, r, a, c);
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar(C::QREADY));
       float m_ref = -INFINITY, l = 0.f;
       for (int j = 0; j < nt; ++j, ++n) {
         if (!(ok = wait(C::sfull(t), n & 1, n))) break;
@@ -436,11 +409,12 @@ __global__ void __launch_bounds__(384, 1)
         mbar_arrive(bar(C::pready(t)));
       }
       if (!ok) break;
-      // Output rows of block t: O / l -> 16-bit -> O[b, row, h, :].
+      // Output rows of block 2·pr + t: O / l -> 16-bit, staged in that block's
+      // Q tile (this warp's 32 rows in its own 4 KB), then written to
+      // O[b, row, h, :] as whole 128-byte rows, 8 lanes per row.
       if (!(ok = wait(C::oready(t), (n - 1) & 1, n))) break;
       tc_fence_after();
       const float inv = 1.f / l;
-      const int row = (2 * pr + t) * 128 + r;
       uint32_t o0[32], o1[32];
       tmem_ld32(tO, o0);
       tmem_ld32(tO + 32, o1);
@@ -448,18 +422,30 @@ __global__ void __launch_bounds__(384, 1)
       tmem_ld_wait(o1);
       tc_fence_before();
       mbar_arrive(bar(C::ofree(t)));
-      if (row < p.S) {
-        uint32_t pk[32];
+      uint32_t pk[32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack2<BF16>(__uint_as_float(o0[2 * i]) * inv, __uint_as_float(o0[2 * i + 1]) * inv);
+      for (int i = 0; i < 16; ++i)
+        pk[i] = pack2<BF16>(__uint_as_float(o0[2 * i]) * inv, __uint_as_float(o0[2 * i + 1]) * inv);
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[16 + i] = pack2<BF16>(__uint_as_float(o1[2 * i]) * inv, __uint_as_float(o1[2 * i + 1]) * inv);
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
-                                              (static_cast<long long>(b) * p.S + row) * p.D + hh * 64);
+      for (int i = 0; i < 16; ++i)
+        pk[16 + i] = pack2<BF16>(__uint_as_float(o1[2 * i]) * inv, __uint_as_float(o1[2 * i + 1]) * inv);
+      if (!(ok = wait(C::QFREE, pr & 1, n))) break;  // the pair's Q·K^T products no longer read its Q tiles
+      uint8_t* stage = smem + C::OFF_Q + (2 * pr + t) * C::TILE + wq * (32 * 128);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+      for (int u = 0; u < 8; ++u)
+        *reinterpret_cast<uint4*>(stage + lane * 128 + ((u ^ (lane & 7)) << 4)) =
+            make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+      __syncwarp();
+      const int row0 = (2 * pr + t) * 128 + static_cast<int>(wq * 32u);
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int rr = it * 4 + static_cast<int>(lane >> 3), u = static_cast<int>(lane & 7);
+        if (row0 + rr < p.S) {
+          const uint4 v = *reinterpret_cast<const uint4*>(stage + rr * 128 + ((u ^ (rr & 7)) << 4));
+          uint16_t* dst = static_cast<uint16_t*>(p.o) + (static_cast<long long>(b) * p.S + row0 + rr) * p.D +
+                          hh * 64 + u * 8;
+          *reinterpret_cast<uint4*>(dst) = v;
+        }
       }
     }
   }

@@ -81,9 +81,7 @@ __device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity, const W
   }
 }
 
-// The same loop out of line, to keep it out of hot code.  Kernels that move
-// registers between warpgroups (setmaxnreg) cannot call out-of-line code from
-// the regions with a changed register count and use the inline form.
+// The same loop out of line, to keep it out of hot code.
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtx& w,
                                                    uint32_t code, bool honor_abort = true) {
   return mbar_poll(bar, parity, w, code, honor_abort);
@@ -377,22 +375,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
 
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-// Register split between warpgroups (setmaxnreg).  Every thread of a
-// warpgroup (four consecutive warps starting at a multiple of four) must
-// execute the same instruction, so a CTA using it must consist of whole
-// warpgroups.  .inc waits until the CTA's pool (threads x registers per
-// thread at launch) has room, so the shares must add up to no more than it.
-template <int N>
-__device__ __forceinline__ void reg_alloc() {
-  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg count");
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <int N>
-__device__ __forceinline__ void reg_dealloc() {
-  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg count");
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // --------------------------------------------------------- arithmetic ----

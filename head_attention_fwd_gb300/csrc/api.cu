@@ -6,6 +6,7 @@
 
 #include <math.h>
 #include <stdlib.h>
+#include <string.h>
 #include <unistd.h>
 
 #include <atomic>
@@ -225,6 +226,29 @@ void o_strides(int layout, long long H, long long S, long long d, long long rs, 
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Whether a 16-bit problem runs on the resident-tile kernel (fused.cu,
+// attention only): d = 64 and S <= 512, where each (batch, head) fits in
+// shared memory and the streaming kernel's per-item start and drain dominate
+// its few key tiles.  The resident kernel runs one CTA per (batch, head) and
+// its pairs of 128-row blocks one after the other; the streaming kernel spreads
+// the pairs (its items) over the SMs.  Resident is taken when its waves times
+// pairs per head do not exceed the streaming kernel's waves of items
+// (measured on GB300: B8 h12 S512 14.2 against 16.2 us, B8 h16 S512 14.3
+// against 15.2, B4 h16 S256 5.9 against 6.7; the rule sends B16 h12 S512,
+// 27.2 against 22.8, and B2 h16 S384, 11.2 against 7.7, to the streaming
+// kernel).  ATTN_RESIDENT=never sends every problem to the streaming kernel
+// and ATTN_RESIDENT=force every d = 64, S <= 512 one to the resident kernel
+// (the tests cover both kernels on the same shapes).
+bool resident_pays(int B, int h, int S, int d, int sms) {
+  if (d != 64 || S > 512 || sms < 1) return false;
+  const char* env = getenv("ATTN_RESIDENT");
+  if (env && strcmp(env, "never") == 0) return false;
+  if (env && strcmp(env, "force") == 0) return true;
+  const long long heads = static_cast<long long>(B) * h;
+  const long long pairs = ((S + 127) / 128 + 1) / 2;
+  return (heads + sms - 1) / sms * pairs <= (heads * pairs + sms - 1) / sms;
+}
+
 // Flash launch on tensors of a [B,H,S,d] problem; inputs and output may have
 // different row strides (rs_in, rs_out: layout 1 only).  Layout
 // ATTN_LAYOUT_GROUPED takes hg heads per group ([B,H/hg,S,hg,d]).
@@ -234,6 +258,29 @@ int run_flash(const void* q, const void* k, const void* v, void* o, float* lse, 
               int d, float scale, int layout, long long hg, int dtype, long long rs_in,
               long long rs_out, const DeviceState* ds, cudaStream_t st, void* scratch = nullptr,
               size_t scratch_bytes = 0) {
+  if (layout != ATTN_LAYOUT_GROUPED && resident_pays(B, h, S, d, ds->num_sms)) {
+    // d = 64, S <= 512: one CTA per (batch, head) with the head's Q, K, V
+    // resident in shared memory (no per-item pipeline start and drain).
+    attn::FusedLaunch r;
+    int hs = 0;
+    int rc2 = make_map(&r.t0, q, dtype, layout, B, h, S, d, rs_in, 128, &hs);
+    if (!rc2) rc2 = make_map(&r.t1, k, dtype, layout, B, h, S, d, rs_in, 128, &hs);
+    if (!rc2) rc2 = make_map(&r.t2, v, dtype, layout, B, h, S, d, rs_in, 128, &hs);
+    if (rc2) return rc2;
+    r.project = false;
+    r.o = o;
+    r.lse = lse;
+    o_strides(layout, h, S, d, rs_out, &r.o_sb, &r.o_sh, &r.o_ss);
+    r.B = B, r.S = S, r.H = h, r.D = h * d;
+    r.hs_swap = hs;
+    r.bf16 = dtype == ATTN_BF16;
+    r.scale = scale;
+    r.status = ds->status;
+    r.limit = wait_limit();
+    (void)scratch;
+    (void)scratch_bytes;
+    return to_rc(attn::launch_fused_qkv_attn(r, st));
+  }
   attn::FlashLaunch a;
   int rc = ATTN_OK;
   a.grouped = layout == ATTN_LAYOUT_GROUPED;
@@ -603,7 +650,7 @@ int qkv_proj_attn_fused(const void* x, const void* w_qkv, void* o, int B, int S,
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * e, static_cast<cuuint64_t>(S) * D * e};
     cuuint32_t box[3] = {64, 128, 1}, estr[3] = {1, 1, 1};
-    if (g_encode(&a.tx, dt, 3, const_cast<void*>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    if (g_encode(&a.t0, dt, 3, const_cast<void*>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return ATTN_E_DEVICE;
@@ -612,13 +659,18 @@ int qkv_proj_attn_fused(const void* x, const void* w_qkv, void* o, int B, int S,
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(3LL * D), static_cast<cuuint64_t>(D)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(3LL * D) * e};
     cuuint32_t box[2] = {64, 64}, estr[2] = {1, 1};
-    if (g_encode(&a.tw, dt, 2, const_cast<void*>(w_qkv), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    if (g_encode(&a.t1, dt, 2, const_cast<void*>(w_qkv), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return ATTN_E_DEVICE;
   }
+  a.t2 = a.t1;  // unused by the projection form
+  a.project = true;
   a.o = o;
-  a.B = B, a.S = S, a.H = h;
+  a.lse = nullptr;
+  a.o_ss = D, a.o_sh = 64, a.o_sb = static_cast<long long>(S) * D;  // [B, S, h, 64]
+  a.B = B, a.S = S, a.H = h, a.D = D;
+  a.hs_swap = 0;
   a.bf16 = dtype == ATTN_BF16;
   a.scale = 1.0f / sqrtf(64.0f);
   a.status = ds->status;

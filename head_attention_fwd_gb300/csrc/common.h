@@ -61,14 +61,23 @@ FlashScratch flash_scratch_layout(int d, int grid);
 
 cudaError_t launch_flash_fwd(const FlashLaunch& a, const FlashPlan& plan, cudaStream_t st);
 
-// Single-kernel QKV projection + attention (fused.cu): one CTA per (batch,
-// head), d = 64, S <= 512.  tx: X [B, S, D] as a 3-d map (D, S, B), box
-// 64 x 128 x 1; tw: W_qkv [D, 3D] as a 2-d map (3D, D), box 64 x 64; both
-// 128-byte swizzled.  o: [B, S, H, 64].
+// Resident-tile attention for d = 64, S <= 512 (fused.cu): one CTA per
+// (batch, head) holds the head's Q, K, V tiles in shared memory.
+// project = true: the single-kernel QKV projection + attention; t0: X
+//   [B, S, D] as a 3-d map (D, S, B), box 64 x 128 x 1; t1: W_qkv [D, 3D] as a
+//   2-d map (3D, D), box 64 x 64.
+// project = false: attention on existing Q, K, V; t0, t1, t2: the 4-d maps of
+//   make_map (box 64 x 128 rows), hs_swap as there.
+// Both 128-byte swizzled.  Output element strides o_sb / o_sh / o_ss (batch,
+// head, position); lse [B, H, S] or null.
 struct FusedLaunch {
-  CUtensorMap tx, tw;
+  CUtensorMap t0, t1, t2;
+  bool project;
   void* o;
-  int B, S, H;
+  float* lse;
+  long long o_sb, o_sh, o_ss;
+  int B, S, H, D;
+  int hs_swap;
   bool bf16;
   float scale;
   unsigned* status;

@@ -60,7 +60,7 @@ struct FCfg {
   static constexpr uint32_t OFF_R = MAXT * TILE;         // projection ring (overlaps K, V)
   static constexpr uint32_t STAGE = MAXT * TILE + 2 * WCH;  // X tiles of every block + one or two weight chunks
   static constexpr uint32_t OFF_BAR = OFF_R + 2 * STAGE;
-  static constexpr int NBAR = 20;
+  static constexpr int NBAR = 24;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t SMEM = OFF_MISC + 16 + 1024;
   static constexpr int THREADS = 384;
@@ -74,15 +74,20 @@ struct FCfg {
   __host__ __device__ static constexpr int pready(int t) { return 14 + t; }
   __host__ __device__ static constexpr int oready(int t) { return 16 + t; }
   __host__ __device__ static constexpr int ofree(int t) { return 18 + t; }
+  // attention only: K and V tile j landed (the Q tiles of pair pr use full(pr))
+  __host__ __device__ static constexpr int kvfull(int j) { return 20 + j; }
 };
 static_assert(FCfg::OFF_R + 2 * FCfg::STAGE <= FCfg::OFF_BAR && FCfg::OFF_V + FCfg::MAXT * FCfg::TILE <= FCfg::OFF_BAR,
               "buffers inside the shared-memory budget");
 static_assert(FCfg::SMEM <= 227 * 1024, "shared memory budget");
 
 struct FParams {
-  void* o;                 // [B, S, h, 64]
-  int S, H, D;             // sequence length, heads, model width (= H * 64)
-  int nkc;                 // D / 64 k-chunks
+  void* o;                 // output, element strides below (feature stride 1)
+  float* lse;              // [B, H, S] fp32 or null
+  long long o_sb, o_sh, o_ss;  // batch, head, position
+  int S, H, D;             // sequence length, heads, model width (projection: H * 64)
+  int nkc;                 // projection: D / 64 k-chunks
+  int hs_swap;             // attention only: maps (d, H, S, B) instead of (d, S, H, B)
   float c;                 // softmax scale * log2(e)
   unsigned* status;
   long long limit;
@@ -109,10 +114,14 @@ __device__ __forceinline__ void store_row_swizzled(uint8_t* tile, int r, const u
         make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
 }
 
-template <bool BF16>
+// PROJ: the projection phases run first (t0 = X, t1 = W_qkv).  Otherwise the
+// kernel is the attention alone on Q, K, V that already exist (t0, t1, t2,
+// 4-d maps (d, S, H, B) or (d, H, S, B)): they are loaded straight into the
+// same resident tiles.
+template <bool BF16, bool PROJ>
 __global__ void __launch_bounds__(384, 1)
     fused_qkv_attn_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant__ CUtensorMap tw,
-                          const __grid_constant__ FParams p) {
+                          const __grid_constant__ CUtensorMap tv, const __grid_constant__ FParams p) {
   using C = FCfg;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -138,6 +147,7 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(bar(C::KVREADY), 256);
     mbar_init(bar(C::QFREE), 1);
     mbar_init(bar(C::DRAIN), 1);
+    for (int j = 0; j < C::MAXT; ++j) mbar_init(bar(C::kvfull(j)), 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(C::sfull(t)), 1);
       mbar_init(bar(C::sconsumed(t)), 128);
@@ -171,10 +181,39 @@ __global__ void __launch_bounds__(384, 1)
     if (lane == 0) {
       prefetch_tmap(&tx);
       prefetch_tmap(&tw);
+      if (!PROJ) prefetch_tmap(&tv);
     }
     bool ok = true;
     int g = 0;  // ring loads issued (both phases)
-    for (int ph = 0; ph < 2 && ok; ++ph) {
+    if constexpr (!PROJ) {
+      // The first pair's Q tiles, then K and V tile by tile, then the second
+      // pair's Q tiles (rows past S read as zeros), each group on its own
+      // barrier so that the attention starts once its first tiles are in.
+      if (lane == 0) {
+        auto load = [&](uint32_t dst, const CUtensorMap* m, uint32_t mbar, int row) {
+          if (p.hs_swap)
+            tma_load_4d(dst, m, mbar, 0, hh, row, b);
+          else
+            tma_load_4d(dst, m, mbar, 0, row, hh, b);
+        };
+        auto load_q = [&](int pr) {
+          mbar_expect_tx(bar(C::full(pr)), 2 * C::TILE);
+          for (int qb = 2 * pr; qb < 2 * pr + 2; ++qb)
+            load(sb + C::OFF_Q + qb * C::TILE, &tx, bar(C::full(pr)), qb * 128);
+        };
+        load_q(0);
+        for (int j = 0; j < nt; ++j) {
+          mbar_expect_tx(bar(C::kvfull(j)), 2 * C::TILE);
+          load(sb + C::OFF_K + j * C::TILE, &tw, bar(C::kvfull(j)), j * 128);
+          load(sb + C::OFF_V + j * C::TILE, &tv, bar(C::kvfull(j)), j * 128);
+        }
+        if (npair > 1) load_q(1);
+      }
+      // Every copy lands before the CTA can exit, even if another role gives up.
+      for (int pr = 0; pr < npair; ++pr) mbar_wait_slow(bar(C::full(pr)), 0, wc, 0, false);
+      for (int j = 0; j < nt; ++j) mbar_wait_slow(bar(C::kvfull(j)), 0, wc, 0, false);
+    }
+    for (int ph = 0; PROJ && ph < 2 && ok; ++ph) {
       for (int kc = 0; kc < p.nkc; ++kc, ++g) {
         const int s = g & 1, u = g >> 1;
         if (u > 0 && !(ok = mbar_wait_warp(bar(C::empty(s)), (u - 1) & 1, wc, fcode(ROLE_LOAD, g)))) break;
@@ -207,7 +246,7 @@ __global__ void __launch_bounds__(384, 1)
     auto commit = [&](int i) { mma_commit_elect(bar(i)); };
     bool ok = true;
     int g = 0;
-    for (int ph = 0; ph < 2 && ok; ++ph) {
+    for (int ph = 0; PROJ && ph < 2 && ok; ++ph) {
       // Phase KV overwrites the Q accumulators: only once they are in shared memory.
       if (ph == 1 && !(ok = wait(C::QREADY, 0, 0))) break;
       for (int kc = 0; kc < p.nkc; ++kc, ++g) {
@@ -227,7 +266,7 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (ok) commit(ph == 0 ? C::QACC : C::KVACC);
     }
-    if (ok) ok = wait(C::KVREADY, 0, 0);
+    if (PROJ && ok) ok = wait(C::KVREADY, 0, 0);
     auto qk = [&](int t, int qb, int j) {  // S_t = Q_qb · K_j^T
       const uint64_t dq = sdesc_sw128(sb + C::OFF_Q + qb * C::TILE, 16, 1024);
       const uint64_t dk = sdesc_sw128(sb + C::OFF_K + j * C::TILE, 16, 1024);
@@ -244,6 +283,7 @@ __global__ void __launch_bounds__(384, 1)
     };
     uint32_t n = 0;  // key tiles of both blocks done (attention barrier phases)
     for (int pr = 0; pr < npair && ok; ++pr) {
+      if (!PROJ && !(ok = wait(C::full(pr), 0, pr) && wait(C::kvfull(0), 0, 0))) break;
       tc_fence_after();
       qk(0, 2 * pr, 0);
       commit(C::sfull(0));
@@ -253,6 +293,7 @@ __global__ void __launch_bounds__(384, 1)
         for (int t = 0; t < 2; ++t) {
           if (!(ok = wait(C::sconsumed(t), n & 1, n))) break;
           if (j + 1 < nt) {
+            if (!PROJ && t == 0 && !(ok = wait(C::kvfull(j + 1), 0, j + 1))) break;
             tc_fence_after();
             qk(t, 2 * pr + t, j + 1);
             commit(C::sfull(t));
@@ -284,8 +325,8 @@ __global__ void __launch_bounds__(384, 1)
     };
     // Phase Q epilogue: warpgroup t rounds blocks t and t + 2 (a block past the
     // sequence that a pair still needs gets zeros).
-    bool ok = wait(C::QACC, 0, 0);
-    if (ok) {
+    bool ok = !PROJ || wait(C::QACC, 0, 0);
+    if (PROJ && ok) {
       tc_fence_after();
       for (int qb = t; qb < 2 * npair; qb += 2) {
         uint32_t a[32], c[32];
@@ -305,7 +346,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_arrive(bar(C::QREADY));
       ok = wait(C::KVACC, 0, 0);
     }
-    if (ok) {
+    if (PROJ && ok) {
       // Phase KV epilogue: row r of every block, K (t = 0) or V (t = 1) half.
       tc_fence_after();
       uint8_t* dst = smem + (t == 0 ? C::OFF_K : C::OFF_V);
@@ -429,6 +470,9 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
       for (int i = 0; i < 16; ++i)
         pk[16 + i] = pack2<BF16>(__uint_as_float(o1[2 * i]) * inv, __uint_as_float(o1[2 * i + 1]) * inv);
+      const int my_row = (2 * pr + t) * 128 + r;
+      if (p.lse && my_row < p.S)
+        p.lse[(static_cast<long long>(b) * p.H + hh) * p.S + my_row] = (m_ref + log2f(l)) * 0.6931471805599453f;
       if (!(ok = wait(C::QFREE, pr & 1, n))) break;  // the pair's Q·K^T products no longer read its Q tiles
       uint8_t* stage = smem + C::OFF_Q + (2 * pr + t) * C::TILE + wq * (32 * 128);
 #pragma unroll
@@ -442,8 +486,8 @@ __global__ void __launch_bounds__(384, 1)
         const int rr = it * 4 + static_cast<int>(lane >> 3), u = static_cast<int>(lane & 7);
         if (row0 + rr < p.S) {
           const uint4 v = *reinterpret_cast<const uint4*>(stage + rr * 128 + ((u ^ (rr & 7)) << 4));
-          uint16_t* dst = static_cast<uint16_t*>(p.o) + (static_cast<long long>(b) * p.S + row0 + rr) * p.D +
-                          hh * 64 + u * 8;
+          uint16_t* dst = static_cast<uint16_t*>(p.o) + b * p.o_sb + hh * p.o_sh +
+                          static_cast<long long>(row0 + rr) * p.o_ss + u * 8;
           *reinterpret_cast<uint4*>(dst) = v;
         }
       }
@@ -458,17 +502,22 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <bool BF16>
+template <bool BF16, bool PROJ>
 cudaError_t launch_fused_t(const FusedLaunch& a, cudaStream_t st) {
-  auto kern = fused_qkv_attn_kernel<BF16>;
+  auto kern = fused_qkv_attn_kernel<BF16, PROJ>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FCfg::SMEM);
   if (e != cudaSuccess) return e;
   FParams p{};
   p.o = a.o;
+  p.lse = a.lse;
+  p.o_sb = a.o_sb;
+  p.o_sh = a.o_sh;
+  p.o_ss = a.o_ss;
   p.S = a.S;
   p.H = a.H;
-  p.D = a.H * 64;
-  p.nkc = p.D / 64;
+  p.D = a.D;
+  p.nkc = a.D / 64;
+  p.hs_swap = a.hs_swap;
   p.c = a.scale * kLog2eF;
   p.status = a.status;
   p.limit = a.limit;
@@ -482,7 +531,7 @@ cudaError_t launch_fused_t(const FusedLaunch& a, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, a.tx, a.tw, p);
+  e = cudaLaunchKernelEx(&cfg, kern, a.t0, a.t1, a.t2, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -490,8 +539,11 @@ cudaError_t launch_fused_t(const FusedLaunch& a, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_fused_qkv_attn(const FusedLaunch& a, cudaStream_t st) {
-  if (a.S < 1 || a.S > 512 || a.H < 1 || a.B < 1) return cudaErrorInvalidValue;
-  return a.bf16 ? launch_fused_t<true>(a, st) : launch_fused_t<false>(a, st);
+  if (a.S < 1 || a.S > 512 || a.H < 1 || a.B < 1 || static_cast<long long>(a.B) * a.H > 0x7fffffffLL)
+    return cudaErrorInvalidValue;
+  if (a.project)
+    return a.bf16 ? launch_fused_t<true, true>(a, st) : launch_fused_t<false, true>(a, st);
+  return a.bf16 ? launch_fused_t<true, false>(a, st) : launch_fused_t<false, false>(a, st);
 }
 
 }  // namespace attn

@@ -24,6 +24,14 @@ def dev():
     return gpu_or_skip()
 
 
+@pytest.fixture(autouse=True)
+def streaming_kernel(monkeypatch):
+    """This file covers the streaming kernel (flash_fwd.cu) at small sizes, so
+    d = 64 problems with S <= 512 are kept off the resident-tile kernel here
+    (tests/test_resident_gpu.py covers that one)."""
+    monkeypatch.setenv("ATTN_RESIDENT", "never")
+
+
 @pytest.fixture
 def force_split(monkeypatch):
     """Cut the last wave even where the library's cost rule would not (short

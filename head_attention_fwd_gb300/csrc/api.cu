@@ -266,11 +266,10 @@ int run_flash(const void* q, const void* k, const void* v, void* o, float* lse, 
     int rc2 = make_map(&r.t0, q, dtype, layout, B, h, S, d, rs_in, 128, &hs);
     if (!rc2) rc2 = make_map(&r.t1, k, dtype, layout, B, h, S, d, rs_in, 128, &hs);
     if (!rc2) rc2 = make_map(&r.t2, v, dtype, layout, B, h, S, d, rs_in, 128, &hs);
+    if (!rc2) rc2 = make_map(&r.to, o, dtype, layout, B, h, S, d, rs_out, 128, &r.o_swap);
     if (rc2) return rc2;
     r.project = false;
-    r.o = o;
     r.lse = lse;
-    o_strides(layout, h, S, d, rs_out, &r.o_sb, &r.o_sh, &r.o_ss);
     r.B = B, r.S = S, r.H = h, r.D = h * d;
     r.hs_swap = hs;
     r.bf16 = dtype == ATTN_BF16;
@@ -665,10 +664,10 @@ int qkv_proj_attn_fused(const void* x, const void* w_qkv, void* o, int B, int S,
       return ATTN_E_DEVICE;
   }
   a.t2 = a.t1;  // unused by the projection form
+  // O [B, S, h, 64]: the head-interleaved layout with row stride D
+  if ((rc = make_map(&a.to, o, dtype, ATTN_LAYOUT_BSHD, B, h, S, 64, D, 128, &a.o_swap))) return rc;
   a.project = true;
-  a.o = o;
   a.lse = nullptr;
-  a.o_ss = D, a.o_sh = 64, a.o_sb = static_cast<long long>(S) * D;  // [B, S, h, 64]
   a.B = B, a.S = S, a.H = h, a.D = D;
   a.hs_swap = 0;
   a.bf16 = dtype == ATTN_BF16;

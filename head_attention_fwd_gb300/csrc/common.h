@@ -68,14 +68,13 @@ cudaError_t launch_flash_fwd(const FlashLaunch& a, const FlashPlan& plan, cudaSt
 //   2-d map (3D, D), box 64 x 64.
 // project = false: attention on existing Q, K, V; t0, t1, t2: the 4-d maps of
 //   make_map (box 64 x 128 rows), hs_swap as there.
-// Both 128-byte swizzled.  Output element strides o_sb / o_sh / o_ss (batch,
-// head, position); lse [B, H, S] or null.
+// to: the output O as a 4-d map of the same form (o_swap like hs_swap).
+// All 128-byte swizzled.  lse [B, H, S] or null.
 struct FusedLaunch {
-  CUtensorMap t0, t1, t2;
+  CUtensorMap t0, t1, t2, to;
   bool project;
-  void* o;
   float* lse;
-  long long o_sb, o_sh, o_ss;
+  int o_swap;
   int B, S, H, D;
   int hs_swap;
   bool bf16;

@@ -60,7 +60,7 @@ struct FCfg {
   static constexpr uint32_t OFF_R = MAXT * TILE;         // projection ring (overlaps K, V)
   static constexpr uint32_t STAGE = MAXT * TILE + 2 * WCH;  // X tiles of every block + one or two weight chunks
   static constexpr uint32_t OFF_BAR = OFF_R + 2 * STAGE;
-  static constexpr int NBAR = 24;
+  static constexpr int NBAR = 26;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t SMEM = OFF_MISC + 16 + 1024;
   static constexpr int THREADS = 384;
@@ -76,15 +76,16 @@ struct FCfg {
   __host__ __device__ static constexpr int ofree(int t) { return 18 + t; }
   // attention only: K and V tile j landed (the Q tiles of pair pr use full(pr))
   __host__ __device__ static constexpr int kvfull(int j) { return 20 + j; }
+  // output rows of query block t of the current pair staged in shared memory
+  __host__ __device__ static constexpr int ostaged(int t) { return 24 + t; }
 };
 static_assert(FCfg::OFF_R + 2 * FCfg::STAGE <= FCfg::OFF_BAR && FCfg::OFF_V + FCfg::MAXT * FCfg::TILE <= FCfg::OFF_BAR,
               "buffers inside the shared-memory budget");
 static_assert(FCfg::SMEM <= 227 * 1024, "shared memory budget");
 
 struct FParams {
-  void* o;                 // output, element strides below (feature stride 1)
   float* lse;              // [B, H, S] fp32 or null
-  long long o_sb, o_sh, o_ss;  // batch, head, position
+  int o_swap;              // output map dims (d, H, S, B) instead of (d, S, H, B)
   int S, H, D;             // sequence length, heads, model width (projection: H * 64)
   int nkc;                 // projection: D / 64 k-chunks
   int hs_swap;             // attention only: maps (d, H, S, B) instead of (d, S, H, B)
@@ -121,7 +122,8 @@ __device__ __forceinline__ void store_row_swizzled(uint8_t* tile, int r, const u
 template <bool BF16, bool PROJ>
 __global__ void __launch_bounds__(384, 1)
     fused_qkv_attn_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant__ CUtensorMap tw,
-                          const __grid_constant__ CUtensorMap tv, const __grid_constant__ FParams p) {
+                          const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
+                          const __grid_constant__ FParams p) {
   using C = FCfg;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -154,6 +156,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(bar(C::pready(t)), 128);
       mbar_init(bar(C::oready(t)), 1);
       mbar_init(bar(C::ofree(t)), 128);
+      mbar_init(bar(C::ostaged(t)), 128);
     }
   }
   if (warp == 9) {
@@ -450,9 +453,10 @@ __global__ void __launch_bounds__(384, 1)
         mbar_arrive(bar(C::pready(t)));
       }
       if (!ok) break;
-      // Output rows of block 2·pr + t: O / l -> 16-bit, staged in that block's
-      // Q tile (this warp's 32 rows in its own 4 KB), then written to
-      // O[b, row, h, :] as whole 128-byte rows, 8 lanes per row.
+      // Output rows of block 2·pr + t: O / l -> 16-bit, written into that
+      // block's Q tile (free once the pair's Q·K^T products are done) in the
+      // 128-byte-swizzled layout, then stored by one TMA bulk copy while the
+      // warps go on with the next pair.
       if (!(ok = wait(C::oready(t), (n - 1) & 1, n))) break;
       tc_fence_after();
       const float inv = 1.f / l;
@@ -463,35 +467,31 @@ __global__ void __launch_bounds__(384, 1)
       tmem_ld_wait(o1);
       tc_fence_before();
       mbar_arrive(bar(C::ofree(t)));
-      uint32_t pk[32];
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        pk[i] = pack2<BF16>(__uint_as_float(o0[2 * i]) * inv, __uint_as_float(o0[2 * i + 1]) * inv);
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        pk[16 + i] = pack2<BF16>(__uint_as_float(o1[2 * i]) * inv, __uint_as_float(o1[2 * i + 1]) * inv);
-      const int my_row = (2 * pr + t) * 128 + r;
+      for (int i = 0; i < 32; ++i) {
+        o0[i] = __float_as_uint(__uint_as_float(o0[i]) * inv);
+        o1[i] = __float_as_uint(__uint_as_float(o1[i]) * inv);
+      }
+      const int blk = 2 * pr + t;
+      const int my_row = blk * 128 + r;
       if (p.lse && my_row < p.S)
         p.lse[(static_cast<long long>(b) * p.H + hh) * p.S + my_row] = (m_ref + log2f(l)) * 0.6931471805599453f;
       if (!(ok = wait(C::QFREE, pr & 1, n))) break;  // the pair's Q·K^T products no longer read its Q tiles
-      uint8_t* stage = smem + C::OFF_Q + (2 * pr + t) * C::TILE + wq * (32 * 128);
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        *reinterpret_cast<uint4*>(stage + lane * 128 + ((u ^ (lane & 7)) << 4)) =
-            make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-      __syncwarp();
-      const int row0 = (2 * pr + t) * 128 + static_cast<int>(wq * 32u);
-#pragma unroll
-      for (int it = 0; it < 8; ++it) {
-        const int rr = it * 4 + static_cast<int>(lane >> 3), u = static_cast<int>(lane & 7);
-        if (row0 + rr < p.S) {
-          const uint4 v = *reinterpret_cast<const uint4*>(stage + rr * 128 + ((u ^ (rr & 7)) << 4));
-          uint16_t* dst = static_cast<uint16_t*>(p.o) + b * p.o_sb + hh * p.o_sh +
-                          static_cast<long long>(row0 + rr) * p.o_ss + u * 8;
-          *reinterpret_cast<uint4*>(dst) = v;
-        }
+      store_row_swizzled<BF16>(smem + C::OFF_Q + blk * C::TILE, r, o0, o1);
+      fence_proxy_async_smem();
+      mbar_arrive(bar(C::ostaged(t)));
+      // The warpgroup's first warp waits (bounded, warp-uniform) for the
+      // block's 128 rows; one of its threads stores them.
+      if (wq == 0 && !(ok = wait(C::ostaged(t), pr & 1, pr))) break;
+      if (r == 0 && blk * 128 < p.S) {
+        if (p.o_swap)
+          tma_store_4d(&to, sb + C::OFF_Q + blk * C::TILE, 0, hh, blk * 128, b);
+        else
+          tma_store_4d(&to, sb + C::OFF_Q + blk * C::TILE, 0, blk * 128, hh, b);
+        bulk_commit();
       }
     }
+    if (r == 0) bulk_wait_all();  // the output copies complete before the CTA exits
   }
 
   tc_fence_before();
@@ -508,11 +508,8 @@ cudaError_t launch_fused_t(const FusedLaunch& a, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FCfg::SMEM);
   if (e != cudaSuccess) return e;
   FParams p{};
-  p.o = a.o;
   p.lse = a.lse;
-  p.o_sb = a.o_sb;
-  p.o_sh = a.o_sh;
-  p.o_ss = a.o_ss;
+  p.o_swap = a.o_swap;
   p.S = a.S;
   p.H = a.H;
   p.D = a.D;
@@ -531,7 +528,7 @@ cudaError_t launch_fused_t(const FusedLaunch& a, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, a.t0, a.t1, a.t2, p);
+  e = cudaLaunchKernelEx(&cfg, kern, a.t0, a.t1, a.t2, a.to, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

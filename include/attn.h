@@ -89,6 +89,14 @@ typedef enum { ATTN_KERNEL_NAIVE = 0, ATTN_KERNEL_ONLINE = 1 } attn_kernel;
  * Non-causal: every query attends to all S keys.  All pointers must be
  * 16-byte aligned.  Errors: ATTN_E_NULL, ATTN_E_SHAPE, ATTN_E_ALIGN,
  * ATTN_E_LAYOUT, ATTN_E_DTYPE, ATTN_E_ALIAS, ATTN_E_DEVICE, or a cudaError_t.
+ *
+ * Kernels: 16-bit problems stream K and V through a pipelined kernel; for
+ * d = 64 and S <= 512, when the head count leaves it no more waves of work
+ * than the streaming kernel, one CTA per (batch, head) keeps the head's Q, K
+ * and V resident in shared memory instead (no per-item pipeline start and
+ * drain).  Both compute the same result up to fp32 summation order.  The
+ * environment variable ATTN_RESIDENT=never|force overrides the choice (for
+ * tests and comparisons).
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h, int S,
              int d, float scale, int layout, int dtype, void* stream);
